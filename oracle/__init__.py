@@ -1,0 +1,247 @@
+"""CPU float64 oracle for DSA sparse decode attention (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  It wraps ``sda_oracle.c`` (plain C, float64,
+built with gcc on first use) through ctypes and shares nothing with the CUDA
+library.  Inputs are numpy arrays or CPU torch tensors holding the same bytes
+the GPU path receives: bf16 as raw 16-bit patterns, FP8 E4M3 as raw bytes.
+
+The definition it computes is the one of the vLLM API page
+"vllm.models.step5.nvidia.ops.sparse_decode_attention" (functions
+``sparse_decode_attention``, ``_gate`` and ``sparse_decode_splits``); the C
+file's header lists the readings taken where that page is silent.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sda_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle_sda.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(out_path: str = _LIB_PATH, mutant: int = 0, force: bool = False) -> str:
+    """Compile the oracle (optionally with one planted mistake) and return the .so path."""
+    if (not force and os.path.exists(out_path)
+            and os.path.getmtime(out_path) >= os.path.getmtime(_SRC)):
+        return out_path
+    os.makedirs(os.path.dirname(out_path), exist_ok=True)
+    tmp = out_path + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall",
+           f"-DORACLE_MUTANT={int(mutant)}", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out_path)
+    return out_path
+
+
+def _declare(lib):
+    i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+    common = [vp, i64, i64, i32, i32,            # query, q_s0, q_s1, rows, heads
+              vp, i32, i64, i32, i32,            # cache, fp8, pages, groups, block
+              i64, i64, i64,                     # c_s0, c_s1, c_s2
+              vp, i64, i32,                      # regions, reg_s0, R
+              vp, i64, i32, i32,                 # block_table, bt_s0, table rows, cols
+              vp, vp,                            # positions, active
+              dbl, i32, i32, dbl, dbl]           # scale, query_len, RT, k_scale, v_scale
+    lib.oracle_sparse_decode_attention.argtypes = common + [vp, i64, i64, vp, i32, vp]
+    lib.oracle_sparse_decode_attention.restype = i32
+    lib.oracle_split_partials.argtypes = common + [i32, vp, i32, vp, vp]
+    lib.oracle_split_partials.restype = i32
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_decode.restype = dbl
+    lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_decode.restype = dbl
+    lib.oracle_bf16_round.argtypes = [ctypes.c_float]
+    lib.oracle_bf16_round.restype = ctypes.c_uint16
+    lib.oracle_gate_factor.argtypes = [ctypes.c_uint16]
+    lib.oracle_gate_factor.restype = dbl
+    lib.oracle_sparse_decode_splits.argtypes = [i32]
+    lib.oracle_sparse_decode_splits.restype = i32
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i32
+    lib.oracle_set_num_threads.argtypes = [i32]
+    lib.oracle_set_num_threads.restype = None
+    return lib
+
+
+def load(path: str | None = None):
+    """The oracle library (built on first use).  ``path`` loads another build, e.g. a mutant."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            _lib = _declare(ctypes.CDLL(build()))
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+_ERRORS = {-1: "bad arguments", -2: "region id below -1", -3: "token past the block-table width",
+           -4: "block-table entry is not a page of the cache", -5: "out of host memory"}
+
+
+def _np(x, dtype):
+    """A numpy view of x's bytes as ``dtype`` (torch CPU tensors are reinterpreted, not converted)."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach()
+            if x.device.type != "cpu":
+                raise ValueError("the oracle takes host tensors")
+            if x.dtype in (torch.bfloat16, torch.float16):
+                x = x.view(torch.int16)
+            elif x.dtype in (torch.float8_e4m3fn, torch.bool):
+                x = x.view(torch.uint8)
+            x = x.numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    x = np.asarray(x)
+    if x.dtype.itemsize != np.dtype(dtype).itemsize:
+        raise ValueError(f"expected {np.dtype(dtype)}-sized elements, got {x.dtype}")
+    return x.view(dtype)
+
+
+def _estrides(a):
+    return [s // a.itemsize for s in a.strides]
+
+
+class Problem:
+    """The arguments of one call, as host arrays plus the C argument list."""
+
+    def __init__(self, query, cache, regions, block_table, positions, active, *, scale,
+                 query_len=1, region_tokens=None, k_scale=None, v_scale=None, cache_fp8=None):
+        self.query = _np(query, np.uint16)
+        if cache_fp8 is None:
+            cache_fp8 = _itemsize(cache) == 1
+        self.fp8 = bool(cache_fp8)
+        self.cache = _np(cache, np.uint8 if self.fp8 else np.uint16)
+        self.regions = _np(regions, np.int32)
+        self.block_table = _np(block_table, np.int32)
+        self.positions = np.ascontiguousarray(_np(positions, np.int32))
+        self.active = np.ascontiguousarray(_np(active, np.uint8))
+        rows, heads, dim = self.query.shape
+        pages, groups, block, width = self.cache.shape
+        if dim != 192 or width != 384:
+            raise ValueError("query dim must be 192 and cache rows 384 wide")
+        if self.fp8 and (k_scale is None or v_scale is None):
+            raise ValueError("an FP8 cache needs k_scale and v_scale")
+        self.rows, self.heads, self.groups, self.block = rows, heads, groups, block
+        self.query_len = int(query_len)
+        self.region_tokens = int(region_tokens or block)
+        qs, cs = _estrides(self.query), _estrides(self.cache)
+        if qs[2] != 1 or cs[3] != 1:
+            raise ValueError("inner strides must be 1")
+        rs, bs = _estrides(self.regions), _estrides(self.block_table)
+        if rows and rs[1] != 1 or bs[1] != 1:
+            raise ValueError("regions / block_table rows must be contiguous")
+        self.args = [
+            self.query.ctypes.data, qs[0], qs[1], rows, heads,
+            self.cache.ctypes.data, int(self.fp8), pages, groups, block, cs[0], cs[1], cs[2],
+            self.regions.ctypes.data, rs[0], self.regions.shape[1],
+            self.block_table.ctypes.data, bs[0], self.block_table.shape[0], self.block_table.shape[1],
+            self.positions.ctypes.data, self.active.ctypes.data,
+            float(scale), self.query_len, self.region_tokens,
+            float(k_scale if k_scale is not None else 1.0), float(v_scale if v_scale is not None else 1.0),
+        ]
+
+
+def _itemsize(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            return x.element_size()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(x).itemsize
+
+
+def _rows_arg(row_ids, rows):
+    if row_ids is None:
+        return None, rows
+    ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int32))
+    return ids, len(ids)
+
+
+def sparse_decode_attention(query, cache, regions, block_table, positions, active, *, scale,
+                            query_len=1, region_tokens=None, k_scale=None, v_scale=None,
+                            gate=None, cache_fp8=None, row_ids=None, lib=None) -> np.ndarray:
+    """float64 output [n, heads, 192] for ``row_ids`` (default: every row).
+
+    ``cache_fp8`` defaults to "the cache has 1-byte elements".  ``gate`` is the
+    bf16 [tokens, G * heads] headwise gate or None.  ``lib`` selects another
+    oracle build (used by the pin-strength test)."""
+    lib = lib or load()
+    p = Problem(query, cache, regions, block_table, positions, active, scale=scale,
+                query_len=query_len, region_tokens=region_tokens, k_scale=k_scale,
+                v_scale=v_scale, cache_fp8=cache_fp8)
+    ids, n = _rows_arg(row_ids, p.rows)
+    out = np.zeros((n, p.heads, 192), dtype=np.float64)
+    if gate is not None:
+        g = _np(gate, np.uint16)
+        gs = _estrides(g)
+        gate_args = [g.ctypes.data, gs[0], gs[1]]
+    else:
+        g = None
+        gate_args = [None, 0, 0]
+    rc = lib.oracle_sparse_decode_attention(
+        *p.args, *gate_args, ids.ctypes.data if ids is not None else None, n, out.ctypes.data)
+    if rc:
+        raise OracleError(_ERRORS.get(rc, str(rc)))
+    return out
+
+
+def split_partials(query, cache, regions, block_table, positions, active, *, scale, splits,
+                   query_len=1, region_tokens=None, k_scale=None, v_scale=None,
+                   cache_fp8=None, row_ids=None, lib=None):
+    """(partial [n, S, heads, 192], lse [n, S, heads]) float64 for split-KV chunk s of S."""
+    lib = lib or load()
+    p = Problem(query, cache, regions, block_table, positions, active, scale=scale,
+                query_len=query_len, region_tokens=region_tokens, k_scale=k_scale,
+                v_scale=v_scale, cache_fp8=cache_fp8)
+    ids, n = _rows_arg(row_ids, p.rows)
+    partial = np.zeros((n, splits, p.heads, 192), dtype=np.float64)
+    lse = np.zeros((n, splits, p.heads), dtype=np.float64)
+    rc = lib.oracle_split_partials(*p.args, int(splits), ids.ctypes.data if ids is not None else None,
+                                   n, partial.ctypes.data, lse.ctypes.data)
+    if rc:
+        raise OracleError(_ERRORS.get(rc, str(rc)))
+    return partial, lse
+
+
+def e4m3_decode(code: int, lib=None) -> float:
+    return (lib or load()).oracle_e4m3_decode(code)
+
+
+def bf16_decode(bits: int, lib=None) -> float:
+    return (lib or load()).oracle_bf16_decode(bits)
+
+
+def bf16_round(x: float, lib=None) -> int:
+    return (lib or load()).oracle_bf16_round(x)
+
+
+def gate_factor(bits: int, lib=None) -> float:
+    return (lib or load()).oracle_gate_factor(bits)
+
+
+def sparse_decode_splits(rows: int, lib=None) -> int:
+    return (lib or load()).oracle_sparse_decode_splits(rows)
+
+
+def num_threads() -> int:
+    return load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    load().oracle_set_num_threads(int(n))
