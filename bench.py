@@ -1,0 +1,368 @@
+"""Benchmark: sparse decode rows/s and selected-KV HBM GB/s on one GB300.
+
+One step = one full sparse decode call (split kernel, plus the combine kernel
+when splits > 1) over one batch of a synthetic workload resident in HBM.
+Default workload: "large" (512 requests x G=4 rows, 16 heads, FP8 E4M3
+cache, R=128 regions of 64 tokens, contexts 128K-256K, 2048 rows).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the float64 CPU
+oracle on the same workload instead (the reference arm of this benchmark).
+Multi-GPU (torchrun): every rank runs an independent replica of the
+workload (rows are independent; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_decode_attention_02_gb300 import inputs  # noqa: E402
+
+METRIC = "sparse decode rows/s and selected-KV HBM GB/s (% of GB300 peak), 1 GPU"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="large", choices=inputs.ORDER)
+    ap.add_argument("--splits", type=int, default=None, help="force a split count")
+    ap.add_argument("--requests", type=int, default=None, help="shrink the batch (profiling)")
+    ap.add_argument("--ctx", type=int, nargs=2, default=None, help="context range override (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(args):
+    cfg = inputs.CONFIGS[args.config]
+    changes = {}
+    if args.requests:
+        changes["requests"] = args.requests
+    if args.ctx:
+        changes["ctx"] = tuple(args.ctx)
+    return inputs.scaled(cfg, **changes) if changes else cfg
+
+
+def describe(cfg, w, splits):
+    return {
+        "workload": (f"{cfg.name}: {cfg.requests} requests x query_len {cfg.query_len} x G={cfg.groups} "
+                     f"= {cfg.rows} rows, {cfg.heads} heads x 192, {'FP8 E4M3' if cfg.fp8 else 'bf16'} "
+                     f"cache, block {cfg.block}, R={cfg.num_regions} regions of {cfg.region_tokens} tokens, "
+                     f"context {cfg.ctx}"),
+        "rows": cfg.rows, "heads": cfg.heads, "groups": cfg.groups, "query_len": cfg.query_len,
+        "block": cfg.block, "region_tokens": cfg.region_tokens, "num_regions": cfg.num_regions,
+        "cache_dtype": "fp8_e4m3" if cfg.fp8 else "bf16", "gate": cfg.gate,
+        "inactive_frac": cfg.inactive_frac, "splits": splits, "seed": cfg.seed,
+        "page_pool": int(w.cache.shape[0]),
+    }
+
+
+def visible_tokens(w) -> np.ndarray:
+    """Per row: how many selected tokens are visible (bench accounting only)."""
+    reg = w.regions.cpu().numpy().astype(np.int64)
+    pos = w.positions.cpu().numpy().astype(np.int64)[:, None]
+    RT = w.region_tokens
+    first = reg * RT
+    live = (reg >= 0) & (first <= pos)
+    n = np.where(live, np.minimum(RT, pos - first + 1), 0).sum(1)
+    return n * (w.active.cpu().numpy() != 0)
+
+
+def traffic(w, splits):
+    """(selected K|V bytes, algorithmic bytes) per call."""
+    elt = 1 if w.fp8 else 2
+    vis = visible_tokens(w)
+    kv = int(vis.sum()) * 384 * elt
+    act = int((w.active.cpu().numpy() != 0).sum())
+    H, R = w.heads, w.regions.shape[1]
+    per_row = H * 192 * 2 * 2 + R * 4 + 8 + (H * 2 if w.gate is not None else 0)
+    table = int(np.ceil(vis / max(1, w.block)).sum()) * 4
+    ws = act * splits * H * (192 + 1) * 4 * 2 if splits > 1 else 0
+    return kv, kv + act * per_row + table + ws
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def cpu_baseline(w, n_rows, seed=0):
+    """The float64 oracle on a bounded sample of the workload's rows."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(w.rows, size=min(n_rows, w.rows), replace=False))
+    hp = inputs.host_subset(w, rows)
+    t0 = time.perf_counter()
+    oracle.sparse_decode_attention(hp.query, hp.cache, hp.regions, hp.block_table, hp.positions,
+                                   hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded rows of the same workload ({dt:.2f} s, float64 C, OpenMP over rows)"}
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the CPU float64 oracle, timed on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+    cfg = workload_config(args)
+    w = inputs.make_workload(cfg, "cpu" if not torch.cuda.is_available() else "cuda:0")
+    steps = args.steps or 3
+    n_rows = args.cpu_rows or min(w.rows, 48)
+    samples = []
+    for k in range(args.warmup + steps):
+        rng = np.random.default_rng(1000 + k)
+        rows = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
+        hp = inputs.host_subset(w, rows)
+        t0 = time.perf_counter()
+        oracle.sparse_decode_attention(hp.query, hp.cache, hp.regions, hp.block_table, hp.positions,
+                                       hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
+        if k >= args.warmup:
+            samples.append(time.perf_counter() - t0)
+    total = sum(samples)
+    value = n_rows * steps / total
+    kv, _ = traffic(w, 1)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": describe(cfg, w, 1),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{n_rows} seeded rows per step of the same workload"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "selected_kv_gbs": kv / w.rows * value / 1e9,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "gb300" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import sparse_decode_attention_02_gb300 as sda
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    sda.load()
+    cfg = workload_config(args)
+    w = inputs.make_workload(cfg, dev)
+    splits = args.splits or sda.sparse_decode_splits(w.rows)
+    ws = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8, device=dev)
+    ks = vs = None
+    if w.fp8:
+        ks = torch.tensor([w.k_scale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([w.v_scale], dtype=torch.float32, device=dev)
+    out = torch.empty_like(w.query)
+    kv_bytes, alg_bytes = traffic(w, splits)
+    flush = kv_bytes < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q=w.query, reg=w.regions, bt=w.block_table, pos=w.positions, act=w.active, gate=w.gate, o=out):
+        sda.sparse_decode_attention(q, w.cache, reg, bt, pos, act, o, scale=w.scale,
+                                    query_len=w.query_len, splits=splits, k_scale=ks, v_scale=vs,
+                                    gate=gate, region_tokens=w.region_tokens, workspace=ws, stream=stream)
+
+    steps = args.steps or (2000 if not flush else 400)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region: exactly `steps` calls
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(steps):
+            if flush:
+                scratch.zero_()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    per_launch = [a.elapsed_time(b) for a, b in ev]                 # ms, split (+ combine)
+    kernel_ms = sum(per_launch)
+    region_ms = t_start.elapsed_time(t_end)
+    timed_ms = kernel_ms if flush else region_ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([timed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        timed_ms = float(t.item())
+    flags = sda.read_errors(ws)
+
+    total_rows = w.rows * steps * world
+    value = total_rows / (timed_ms / 1e3)
+    ms_per_step = timed_ms / steps
+    avg_launch_ms = statistics.mean(per_launch)
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / (avg_launch_ms / 1e3) / 1e9
+    kv_gbs = kv_bytes * steps * world / (timed_ms / 1e3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16" if w.fp8 else "bf16", "data": "synthetic",
+        "config": {**describe(cfg, w, splits),
+                   "l2": ("flushed between steps (512 MiB write), per-step CUDA events summed" if flush
+                          else "inputs larger than L2 (selected K|V per step >> 129 MB)"),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "selected_kv_gbs": kv_gbs,
+        "selected_kv_frac_of_peak": kv_gbs / world / peak,
+        "active_rows_per_s": value * float((w.active.cpu().numpy() != 0).mean()),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "sda_split_kernel" + (" + sda_combine_kernel" if splits > 1 else ""),
+                     "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": avg_launch_ms},
+        "gpu_launches": steps * (2 if splits > 1 else 1),
+        "device_flags": flags,
+        "clocks": clocks.summary(),
+    }
+
+    # ---- end to end through the public API: pinned host inputs -> device, call, output -> host
+    if not args.no_e2e:
+        host = {k: v.cpu().pin_memory() for k, v in dict(q=w.query, reg=w.regions, bt=w.block_table,
+                                                          pos=w.positions, act=w.active).items()}
+        if w.gate is not None:
+            host["gate"] = w.gate.cpu().pin_memory()
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = host_out.numel() * host_out.element_size()
+        e2e_steps = max(10, steps // 4)
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            step(**dev_in)
+            host_out.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            if flush:
+                scratch.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        e2e_s = time.perf_counter() - t0
+        line["e2e"] = {"value": w.rows * e2e_steps * world / e2e_s, "unit": "rows/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "note": "host wall clock; includes the L2 flush when flushing"}
+
+    if rank == 0 and world == 1 and not args.no_cpu:
+        n = args.cpu_rows or min(w.rows, 192)
+        line["cpu_baseline"] = cpu_baseline(w, n)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,164 @@
+/*
+ * sdattn.h - C ABI of the GB300 (sm_103a) DSA sparse decode attention library.
+ *
+ * The operation is the one of the vLLM API page
+ * "vllm.models.step5.nvidia.ops.sparse_decode_attention" (function
+ * `sparse_decode_attention` and its module docstring): for every
+ * (token, KV group) row, all query heads of that group attend over only the
+ * row's selected KV regions, read in place from a paged cache through
+ * block_table, with FP8 dequantised, tokens past the row's position masked,
+ * split-KV partials merged through their log-sum-exp, an optional headwise
+ * sigmoid gate applied with bf16 rounding (the page's `_gate`), and inactive
+ * rows cleared.
+ *
+ * Conventions for every entry point:
+ *   - Pointers inside `sda_tensor` are DEVICE pointers of the current CUDA
+ *     device; shapes and strides are in elements (not bytes).
+ *   - The caller owns every buffer.  The library allocates no device memory,
+ *     never synchronises the stream (except sparse_decode_read_errors) and
+ *     returns a status instead of aborting.  A launch is asynchronous: results
+ *     are valid once the stream has reached that point.
+ *   - Inputs are read only; only `output` and `workspace` are written.
+ */
+#ifndef SDATTN_H
+#define SDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDA_OK = 0,
+    SDA_ERR_INVALID = 1,      /* an argument breaks the documented contract            */
+    SDA_ERR_UNSUPPORTED = 2,  /* well formed, but outside what the kernels handle      */
+    SDA_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small            */
+    SDA_ERR_CUDA = 4,         /* a CUDA runtime or driver call failed                  */
+    SDA_ERR_TIMEOUT = 5,      /* device flag: a bounded wait inside a kernel gave up   */
+    SDA_ERR_BOUNDS = 6        /* device flag: an index read from the inputs was bad    */
+} sda_status;
+
+typedef enum {
+    SDA_DTYPE_BF16 = 1,
+    SDA_DTYPE_FP8_E4M3 = 2,   /* OCP E4M3 "fn" (finite, bias 7)                        */
+    SDA_DTYPE_UINT8 = 3,      /* raw bytes; an FP8 cache may be passed as uint8        */
+    SDA_DTYPE_INT32 = 4,
+    SDA_DTYPE_BOOL = 5        /* one byte, nonzero = true                              */
+} sda_dtype;
+
+/* A strided view of device memory.  Unused trailing shape/stride entries are
+ * ignored.  `data` may be NULL only where an argument is documented optional. */
+typedef struct {
+    const void *data;
+    int32_t dtype;            /* sda_dtype */
+    int32_t ndim;
+    int64_t shape[4];
+    int64_t stride[4];        /* in elements */
+} sda_tensor;
+
+/* Device error flags accumulated in the workspace header (bit values). */
+#define SDA_FLAG_BOUNDS  0x1u  /* a region id < -1, a table column past the table width, or a
+                                  table entry outside [0, pages) was met; that piece was skipped */
+#define SDA_FLAG_TIMEOUT 0x2u  /* a pipeline wait exceeded its limit; the row's output is invalid */
+
+/*
+ * Split count per row: start at 1 and double while below 32 and
+ * rows * splits * 2 <= 256, i.e. about 256 split programs per call.
+ * Follows `sparse_decode_splits` on the page named above (the split cannot
+ * follow context length because CUDA graphs are captured per batch size).
+ * rows < 0 returns 1.
+ */
+int sparse_decode_splits(int rows);
+
+/*
+ * Bytes of workspace `sparse_decode_attention` needs for `rows` rows of
+ * `heads` heads with `splits` splits: a 256-byte header (device error flags)
+ * plus, when splits > 1, fp32 partial outputs [rows*splits*heads, 192] and
+ * fp32 log-sum-exps [rows*splits*heads] (the page's `partial` and `lse`).
+ * Returns 0 for arguments out of range.
+ */
+size_t sparse_decode_workspace_bytes(int rows, int heads, int splits);
+
+/*
+ * Sparse decode attention (page above, function `sparse_decode_attention`).
+ *
+ *   query        [rows, H, 192] bf16, stride[2] == 1, H in 1..16.
+ *                rows = tokens * G; row r is KV group r % G of token r / G.
+ *   cache        [pages, G, B, 384] bf16, FP8_E4M3 or UINT8 (E4M3 bytes);
+ *                K in elements 0..191 and V in 192..383 of a token's row.
+ *                stride[3] == 1; any page / group / token strides whose byte
+ *                sizes are multiples of 16 (and a 16-byte aligned base).
+ *   regions      [rows, R] int32, stride[1] == 1.  Region ids of the row, any
+ *                order; -1 marks an unused slot.  Id `id` covers the request's
+ *                logical tokens [id*RT, (id+1)*RT), RT = region_tokens.
+ *   block_table  [requests, W] int32, stride[1] == 1.  Logical block c of
+ *                request q lives in page block_table[q, c].  The G*query_len
+ *                consecutive rows of one request share its table row:
+ *                request = r / (G * query_len).
+ *   positions    [rows] int32: the row's token position (0-based); a token t
+ *                is visible iff t <= position.
+ *   active       [rows] BOOL or UINT8: zero rows are not computed; with
+ *                clear_inactive their output is written as +0.0.
+ *   output       [rows, H, 192] bf16, stride[2] == 1 (written).
+ *   scale        softmax scale applied to q.k (e.g. 1/sqrt(192)).
+ *   query_len    tokens per request (>= 1).
+ *   splits       split-KV programs per row, 1..64 (see sparse_decode_splits).
+ *                Each split takes a contiguous chunk [s*n/S, (s+1)*n/S) of the
+ *                row's live regions; splits > 1 adds the combine kernel.
+ *   k_scale, v_scale  device fp32 scalars; required for an FP8 cache, ignored
+ *                for bf16.  K = decode(byte) * k_scale, V = decode(byte) * v_scale.
+ *   gate         NULL (or data == NULL) for no gate, else [tokens, G*H] bf16:
+ *                head h of row r is multiplied by bf16(sigmoid(gate[r/G,
+ *                (r%G)*H + h])) computed in fp32 (the page's `_gate`).
+ *   clear_inactive  nonzero: inactive rows are written as +0.0; zero: left as is.
+ *   region_tokens   RT; 0 means RT = B.  min(RT, B, 64) must be a multiple of 8
+ *                and divide both RT and B.
+ *   workspace    device buffer of >= sparse_decode_workspace_bytes(rows, H,
+ *                splits) bytes, 256-byte aligned; its first 4 bytes are error
+ *                flags the kernels OR into (zero them once before first use;
+ *                see sparse_decode_read_errors).  Calls that overlap on the
+ *                GPU must not share a workspace.
+ *   stream       cudaStream_t (NULL = legacy default stream).
+ *
+ * Returns SDA_OK after enqueueing the kernels (rows == 0 enqueues nothing),
+ * SDA_ERR_INVALID / SDA_ERR_UNSUPPORTED / SDA_ERR_WORKSPACE without touching
+ * the GPU, or SDA_ERR_CUDA when a launch failed.  Device-side problems are
+ * reported through the workspace flags, never by a trap.
+ *
+ * FP8 note: the kernels convert E4M3 to fp16 exactly; the two NaN codes
+ * (S.1111.111) are not meaningful cache contents and are not special-cased.
+ * The FP8 path multiplies q in fp16, so |q| must stay below 65504.
+ */
+sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *cache,
+                                   const sda_tensor *regions, const sda_tensor *block_table,
+                                   const sda_tensor *positions, const sda_tensor *active,
+                                   const sda_tensor *output, float scale, int query_len,
+                                   int splits, const float *k_scale, const float *v_scale,
+                                   const sda_tensor *gate, int clear_inactive, int region_tokens,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reads the device error flags (SDA_FLAG_*) from a workspace into *flags,
+ * optionally clearing them.  Synchronises `stream` (it must be the stream the
+ * calls ran on).  Returns SDA_ERR_CUDA if a CUDA call failed.
+ */
+sda_status sparse_decode_read_errors(const void *workspace, uint32_t *flags, int clear, void *stream);
+
+/*
+ * Upper bound in nanoseconds for every pipeline wait inside the kernels
+ * (default 1e9).  A wait that runs out sets SDA_FLAG_TIMEOUT, stops the row,
+ * lets in-flight copies land and returns.  Applies to launches made after the
+ * call, process-wide.  Meant for failure-detection tests.
+ */
+void sparse_decode_set_wait_limit_ns(uint64_t ns);
+
+/* A static description of a status code. */
+const char *sparse_decode_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDATTN_H */

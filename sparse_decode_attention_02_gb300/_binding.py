@@ -1,0 +1,190 @@
+"""ctypes binding of libsdattn.so (argument marshalling only).
+
+Every function here turns torch tensors into the C ABI's `sda_tensor`
+descriptors and calls the library; all computation happens in the CUDA
+kernels behind include/sdattn.h.  There is no fallback: if the library is
+missing or fails to load, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsdattn.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "sdattn.h")
+
+SDA_OK, SDA_ERR_INVALID, SDA_ERR_UNSUPPORTED, SDA_ERR_WORKSPACE, SDA_ERR_CUDA, SDA_ERR_TIMEOUT, SDA_ERR_BOUNDS = range(7)
+FLAG_BOUNDS = 0x1
+FLAG_TIMEOUT = 0x2
+
+_DTYPES = {
+    torch.bfloat16: 1,
+    torch.float8_e4m3fn: 2,
+    torch.uint8: 3,
+    torch.int32: 4,
+    torch.bool: 5,
+}
+
+
+class SdaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class SdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"sparse_decode_attention: {message} (status {status})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _declare(lib):
+    P = ctypes.POINTER(SdaTensor)
+    lib.sparse_decode_splits.argtypes = [ctypes.c_int]
+    lib.sparse_decode_splits.restype = ctypes.c_int
+    lib.sparse_decode_workspace_bytes.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.sparse_decode_workspace_bytes.restype = ctypes.c_size_t
+    lib.sparse_decode_attention.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, P,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                            ctypes.c_size_t, ctypes.c_void_p]
+    lib.sparse_decode_attention.restype = ctypes.c_int
+    lib.sparse_decode_read_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32),
+                                              ctypes.c_int, ctypes.c_void_p]
+    lib.sparse_decode_read_errors.restype = ctypes.c_int
+    lib.sparse_decode_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.sparse_decode_set_wait_limit_ns.restype = None
+    lib.sparse_decode_status_string.argtypes = [ctypes.c_int]
+    lib.sparse_decode_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def load(path: str | None = None):
+    """The loaded library.  Raises if it has not been built (see build.py)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with "
+                                  "`python -c 'import __graft_entry__ as g; g.build()'`")
+            _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def declared_functions() -> list[str]:
+    """Names of the entry points include/sdattn.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sparse_decode_\w+)\s*\(", text)))
+
+
+def describe(t: torch.Tensor | None) -> SdaTensor | None:
+    if t is None:
+        return None
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() > 4:
+        raise ValueError("at most 4 dimensions")
+    d = SdaTensor()
+    d.data = t.data_ptr() if t.numel() else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _ref(d):
+    return ctypes.byref(d) if d is not None else None
+
+
+def sparse_decode_splits(rows: int) -> int:
+    return load().sparse_decode_splits(int(rows))
+
+
+def workspace_bytes(rows: int, heads: int, splits: int) -> int:
+    return load().sparse_decode_workspace_bytes(int(rows), int(heads), int(splits))
+
+
+_workspaces: dict = {}
+
+
+def default_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-initialised per-device workspace, grown on demand.  Calls that
+    run concurrently on different streams must pass their own workspace."""
+    key = torch.device(device)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 1 << 12), dtype=torch.uint8, device=key)
+        _workspaces[key] = ws
+    return ws
+
+
+def _scale_ptr(x, device):
+    if x is None:
+        return None, None
+    if not isinstance(x, torch.Tensor):
+        x = torch.tensor([float(x)], dtype=torch.float32, device=device)
+    if x.dtype != torch.float32 or x.device != device or x.numel() != 1:
+        raise ValueError("k_scale / v_scale must be one-element float32 tensors on the query's device")
+    return x.data_ptr(), x
+
+
+def sparse_decode_attention(query, cache, regions, block_table, positions, active, output, *,
+                            scale: float, query_len: int = 1, splits: int | None = None,
+                            clear_inactive: bool = True, k_scale=None, v_scale=None, gate=None,
+                            region_tokens: int = 0, workspace: torch.Tensor | None = None,
+                            stream: torch.cuda.Stream | None = None) -> None:
+    """Sparse decode attention into `output` (see include/sdattn.h for the contract).
+
+    `splits=None` uses the library's split policy.  `k_scale`/`v_scale` are
+    one-element float32 device tensors (python floats are uploaded)."""
+    lib = load()
+    rows, heads = query.shape[0], query.shape[1]
+    if splits is None:
+        splits = lib.sparse_decode_splits(rows)
+    need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
+    if workspace is None:
+        workspace = default_workspace(query.device, need)
+    ks, _keep_k = _scale_ptr(k_scale, query.device)
+    vs, _keep_v = _scale_ptr(v_scale, query.device)
+    descs = [describe(x) for x in (query, cache, regions, block_table, positions, active, output)]
+    gd = describe(gate)
+    s = stream if stream is not None else torch.cuda.current_stream(query.device)
+    rc = lib.sparse_decode_attention(*[_ref(d) for d in descs], float(scale), int(query_len),
+                                     int(splits), ks, vs, _ref(gd), int(bool(clear_inactive)),
+                                     int(region_tokens), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+
+
+def read_errors(workspace: torch.Tensor, clear: bool = False,
+                stream: torch.cuda.Stream | None = None) -> int:
+    """Device error flags (FLAG_BOUNDS | FLAG_TIMEOUT) recorded in a workspace; synchronises."""
+    lib = load()
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    out = ctypes.c_uint32(0)
+    rc = lib.sparse_decode_read_errors(workspace.data_ptr(), ctypes.byref(out), int(clear), s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+    return out.value
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    load().sparse_decode_set_wait_limit_ns(int(ns))
+
+
+def status_string(code: int) -> str:
+    return load().sparse_decode_status_string(int(code)).decode()

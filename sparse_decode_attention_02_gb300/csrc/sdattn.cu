@@ -1,0 +1,1126 @@
+// GB300 (sm_103a) DSA sparse decode attention over a paged KV cache.
+//
+// Implements the operation of the vLLM API page
+// "vllm.models.step5.nvidia.ops.sparse_decode_attention" (function
+// `sparse_decode_attention`, helper `_gate`, policy `sparse_decode_splits`)
+// behind the C ABI declared in include/sdattn.h.
+//
+// Design (one CTA per (row, split) unit; 5 warps):
+//   * warp 4 (producer) compacts the row's live regions, splits them into a
+//     contiguous chunk per split, resolves each region's pages through
+//     block_table and streams "pieces" (runs of P = min(RT, B, 64) tokens of
+//     one page) into a ring of 64-token stages with TMA tensor copies
+//     (128-byte swizzled column bands of the [pages, G, B, 384] cache);
+//   * warps 0-3 (consumers) each own 16 token slots of a stage: QK^T for the
+//     16-head x 192 query tile with mma.sync m16n8k16 (heads are the M
+//     dimension), causal/validity masking, online softmax in fp32, PV with
+//     mma.sync; FP8 bytes are converted to fp16 in registers;
+//   * the epilogue merges the four warps' (max, sum, O) through shared memory
+//     and either writes the gated bf16 output (one split) or the split's fp32
+//     partial output and log-sum-exp for the combine kernel.
+// Every mbarrier wait is bounded; a wait that runs out raises a flag in the
+// workspace header and the CTA winds down after its copies have landed.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "sdattn.h"
+
+namespace {
+
+constexpr int kDim = 192;
+constexpr int kRow = 384;
+constexpr int kMaxHeads = 16;
+constexpr int kSlots = 64;                 // token slots per pipeline stage
+constexpr int kBandBytes = kSlots * 128;   // one 128-byte column band of a stage
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxSplits = 64;
+constexpr int kObufStride = 208;           // floats per head row of the epilogue buffer
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack = 8.0f;      // log2 units a running max may lag the true max
+constexpr size_t kHeaderBytes = 256;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
+
+template <bool FP8>
+struct Traits;
+template <>
+struct Traits<true> {                      // 384 B per token: 3 bands, 4 stages of 24 KB
+    static constexpr int kBands = 3;
+    static constexpr int kStages = 4;
+    static constexpr int kElt = 1;
+};
+template <>
+struct Traits<false> {                     // 768 B per token: 6 bands, 2 stages of 48 KB
+    static constexpr int kBands = 6;
+    static constexpr int kStages = 2;
+    static constexpr int kElt = 2;
+};
+
+template <bool FP8>
+struct Layout {
+    static constexpr int kStageBytes = Traits<FP8>::kBands * kBandBytes;
+    static constexpr int kRing = Traits<FP8>::kStages * kStageBytes;
+    static constexpr int kBarOff = kRing;
+    static constexpr int kHdrOff = kBarOff + 16 * Traits<FP8>::kStages;
+    static constexpr int kCtlOff = kHdrOff + 8 * Traits<FP8>::kStages;
+    static constexpr int kMlOff = kCtlOff + 64;
+    static constexpr int kGammaOff = kMlOff + kConsumerWarps * kMaxHeads * 2 * 4;
+    static constexpr int kQOff = kGammaOff + kMaxHeads * 4;      // Q fragments [12][32] x 16 B
+    static constexpr int kLiveOff = kQOff + 12 * 32 * 16;
+    static_assert(kRing >= kConsumerWarps * kMaxHeads * kObufStride * 4, "epilogue buffer");
+    static size_t bytes(int num_regions) {
+        return 1024 + kLiveOff + 4 * (size_t)((num_regions + 31) & ~31);
+    }
+};
+
+struct Params {
+    const uint16_t *query;
+    int64_t q_s0, q_s1;
+    const int32_t *regions;
+    int64_t reg_s0;
+    const int32_t *block_table;
+    int64_t bt_s0;
+    const int32_t *positions;
+    int64_t pos_s0;
+    const uint8_t *active;
+    int64_t act_s0;
+    uint16_t *output;
+    int64_t o_s0, o_s1;
+    const uint16_t *gate;
+    int64_t g_s0, g_s1;
+    const float *k_scale;
+    const float *v_scale;
+    float *partial;
+    float *lse;
+    unsigned int *flags;
+    long long pages;
+    unsigned long long wait_ns;
+    float scale;
+    int num_regions, table_cols;
+    int rows, heads, groups, block, region_tokens, piece, query_len, splits;
+    int clear_inactive;
+};
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile(
+        "{\n\t.reg .b64 st;\n\t"
+        "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase of `bar` with the given parity; false after limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (global_timer_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, int w, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void consumer_bar()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1,
+                                              uint32_t &r2, uint32_t &r3)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1)
+{
+    if constexpr (FP8) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// Two E4M3 bytes (low byte -> low half) to two fp16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes)
+{
+    uint32_t r;
+    const uint16_t v = static_cast<uint16_t>(two_bytes);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(a), "r"(sel));
+    return r;
+}
+
+template <bool FP8>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    uint32_t r;
+    if constexpr (FP8)
+        asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b)
+{
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// `_gate`: sigmoid in fp32 (1 / (1 + exp(-g)) with a round-to-nearest
+// division), rounded to bf16 and read back as fp32.
+__device__ __forceinline__ float gate_factor(uint16_t g_bits)
+{
+    const float g = bf16_bits_to_float(g_bits);
+    const float sig = __fdiv_rn(1.0f, 1.0f + expf(-g));
+    return __bfloat162float(__float2bfloat16_rn(sig));
+}
+
+// Token slot of k-index n (0..7) inside an 8-slot group.  Pairs of fragment
+// columns (2p, 2p+1) map to slots (p, p+4) so that the eight 16-byte K reads
+// of one shared-memory phase hit eight different swizzled chunks.
+__device__ __forceinline__ int rowmap(int n)
+{
+    return (n >> 1) | ((n & 1) << 2);
+}
+
+// ---------------------------------------------------------------------------
+// Split kernel
+// ---------------------------------------------------------------------------
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 2)
+    sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
+{
+    using T = Traits<FP8>;
+    using L = Layout<FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t full_bar = sbase + L::kBarOff;
+    const uint32_t empty_bar = full_bar + 8 * T::kStages;
+    uint64_t *hdr = reinterpret_cast<uint64_t *>(smem + L::kHdrOff);
+    int *ctl = reinterpret_cast<int *>(smem + L::kCtlOff);
+    float *ml = reinterpret_cast<float *>(smem + L::kMlOff);
+    float *gam = reinterpret_cast<float *>(smem + L::kGammaOff);
+    int *live = reinterpret_cast<int *>(smem + L::kLiveOff);
+    const uint32_t qfrag = sbase + L::kQOff;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x / p.splits;
+    const int split = blockIdx.x - row * p.splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < T::kStages; ++s) {
+            mbar_init(full_bar + 8 * s, 1);
+            mbar_init(empty_bar + 8 * s, kConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    if (warp == kConsumerWarps && lane == 0)
+        prefetch_tmap(&tmap);
+    pdl_launch_dependents();
+    pdl_wait();   // inputs may be written by the previous kernel on the stream
+
+    const bool act = p.active[row * p.act_s0] != 0;
+    const int pos = p.positions[row * p.pos_s0];
+    const int P = p.piece;
+    const int npr = p.region_tokens / P;   // pieces per region
+
+    const int g = lane >> 2;               // fragment row group
+    const int t = lane & 3;                // thread in quad
+
+    if (warp == kConsumerWarps) {
+        // ---- Producer: compact the live regions of this row, in stored order.
+        int n_live = 0;
+        if (act) {
+            const int32_t *reg = p.regions + static_cast<int64_t>(row) * p.reg_s0;
+            for (int j0 = 0; j0 < p.num_regions; j0 += 32) {
+                const int j = j0 + lane;
+                const int id = j < p.num_regions ? reg[j] : -1;
+                if (id < -1)
+                    atomicOr(p.flags, SDA_FLAG_BOUNDS);
+                const bool ok = id >= 0 && static_cast<int64_t>(id) * p.region_tokens <= pos;
+                const unsigned m = __ballot_sync(~0u, ok);
+                if (ok)
+                    live[n_live + __popc(m & ((1u << lane) - 1u))] = id;
+                n_live += __popc(m);
+            }
+        }
+        __syncwarp();
+        const int lo = static_cast<int>(static_cast<int64_t>(split) * n_live / p.splits);
+        const int hi = static_cast<int>(static_cast<int64_t>(split + 1) * n_live / p.splits);
+        long long pieces = 0;
+        for (int i = lo + lane; i < hi; i += 32) {
+            const int64_t first = static_cast<int64_t>(live[i]) * p.region_tokens;
+            pieces += min(static_cast<int64_t>(npr), (pos - first) / P + 1);
+        }
+        for (int o = 16; o; o >>= 1)
+            pieces += __shfl_xor_sync(~0u, pieces, o);
+        if (lane == 0) {
+            ctl[0] = static_cast<int>((pieces * P + kSlots - 1) / kSlots);
+            ctl[1] = lo;
+            ctl[2] = hi;
+        }
+    } else {
+        // ---- Consumers: Q A-fragments into shared memory, in fragment order
+        // ([k-step][lane] x 4 words).  K-step kk of thread t covers the four
+        // dims d0..d0+3 that its K loads deliver (see the QK loop below).
+        const uint16_t *q0 = p.query + static_cast<int64_t>(row) * p.q_s0;
+        const int m0 = g, m1 = g + 8;
+#pragma unroll
+        for (int kk = warp; kk < 12; kk += kConsumerWarps) {
+            int d0;
+            if constexpr (FP8)
+                d0 = 64 * (kk >> 2) + 16 * t + 4 * (kk & 3);
+            else
+                d0 = 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * t + 4 * (kk & 1);
+            float a[2][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int m = r ? m1 : m0;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    a[r][e] = (act && m < p.heads)
+                                  ? bf16_bits_to_float(q0[static_cast<int64_t>(m) * p.q_s1 + d0 + e])
+                                  : 0.0f;
+            }
+            const uint32_t addr = qfrag + (kk * 32 + lane) * 16;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(pack2<FP8>(a[0][0], a[0][1])), "r"(pack2<FP8>(a[1][0], a[1][1])),
+                         "r"(pack2<FP8>(a[0][2], a[0][3])), "r"(pack2<FP8>(a[1][2], a[1][3]))
+                         : "memory");
+        }
+    }
+    __syncthreads();
+    const int n_st = ctl[0];
+
+    if (warp == kConsumerWarps) {
+        // ---- Producer: stream pieces into the stage ring.
+        const int lo = ctl[1], hi = ctl[2];
+        const int64_t req = row / (p.groups * p.query_len);
+        const int grp = row % p.groups;
+        const int32_t *bt = p.block_table + req * p.bt_s0;
+        const int pps = kSlots / P;
+        const uint32_t piece_bytes = static_cast<uint32_t>(P) * kRow * T::kElt;
+        int stage = 0, fill = 0, issued = 0;
+        uint32_t phase = 0;
+        uint64_t mask = 0;
+        bool aborted = false;
+        for (int base = lo; base < hi && !aborted; base += 32) {
+            const int i = base + lane;
+            const bool have_r = i < hi;
+            const int id = have_r ? live[i] : 0;
+            const int64_t first = static_cast<int64_t>(id) * p.region_tokens;
+            const int pc = have_r ? static_cast<int>(min(static_cast<int64_t>(npr), (pos - first) / P + 1)) : 0;
+            for (int j = 0; j < npr && !aborted; ++j) {
+                const bool have = j < pc;
+                const int64_t t0 = first + static_cast<int64_t>(j) * P;
+                const int64_t col = t0 / p.block;
+                const int off = static_cast<int>(t0 - col * p.block);
+                int page = -1;
+                if (have) {
+                    if (col < p.table_cols)
+                        page = bt[col];
+                    if (col >= p.table_cols || page < 0 || page >= p.pages) {
+                        atomicOr(p.flags, SDA_FLAG_BOUNDS);
+                        page = -1;
+                    }
+                }
+                const int nv = have ? static_cast<int>(min(static_cast<int64_t>(P), pos - t0 + 1)) : 0;
+                unsigned bits = __ballot_sync(~0u, have);
+                while (bits) {
+                    const int src = __ffs(bits) - 1;
+                    bits &= bits - 1;
+                    const int pg = __shfl_sync(~0u, page, src);
+                    const int of = __shfl_sync(~0u, off, src);
+                    const int n = __shfl_sync(~0u, nv, src);
+                    if (lane == 0 && !aborted) {
+                        if (fill == 0 && issued >= T::kStages &&
+                            !mbar_wait(empty_bar + 8 * stage, phase ^ 1u, p.wait_ns)) {
+                            atomicOr(p.flags, SDA_FLAG_TIMEOUT);
+                            aborted = true;
+                        }
+                        if (!aborted) {
+                            if (pg >= 0) {
+                                const uint32_t fb = full_bar + 8 * stage;
+                                mbar_expect_tx(fb, piece_bytes);
+                                const uint32_t dst = sbase + stage * L::kStageBytes + fill * P * 128;
+#pragma unroll
+                                for (int b = 0; b < T::kBands; ++b)
+                                    tma_load_4d(dst + b * kBandBytes, &tmap, b * (128 / T::kElt), of,
+                                                grp, pg, fb);
+                                const uint64_t bitsv = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+                                mask |= bitsv << (fill * P);
+                            }
+                            if (++fill == pps) {
+                                hdr[stage] = mask;
+                                mbar_arrive(full_bar + 8 * stage);
+                                ++issued;
+                                fill = 0;
+                                mask = 0;
+                                if (++stage == T::kStages) {
+                                    stage = 0;
+                                    phase ^= 1u;
+                                }
+                            }
+                        }
+                    }
+                    aborted = __shfl_sync(~0u, aborted, 0);
+                }
+            }
+        }
+        if (lane == 0) {
+            if (fill > 0) {   // commit the last, partly filled stage (also after an abort)
+                hdr[stage] = mask;
+                mbar_arrive(full_bar + 8 * stage);
+                ++issued;
+            }
+            // Let every copy this CTA started land before any thread can exit.
+            for (int k = issued > T::kStages ? issued - T::kStages : 0; k < issued; ++k)
+                mbar_wait(full_bar + 8 * (k % T::kStages), static_cast<uint32_t>(k / T::kStages) & 1u,
+                          kDrainLimitNs);
+        }
+        return;
+    }
+
+    // ---- Consumers.
+    const float kfold = FP8 ? __ldg(p.k_scale) : 1.0f;
+    const float vfold = FP8 ? __ldg(p.v_scale) : 1.0f;
+    const float sl2 = p.scale * kLog2e * kfold;
+
+    float o[24][4];
+#pragma unroll
+    for (int n = 0; n < 24; ++n)
+        o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.0f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.0f, 0.0f};
+
+    // Per-lane part of the V ldmatrix addresses: matrix mi = lane / 8 covers
+    // k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of the chunk pair.
+    const int mi = lane >> 3;
+    const int vk = (mi & 1) * 8 + (lane & 7);
+    const int vslot = 16 * warp + (vk & 8) + rowmap(vk & 7);
+    const int vsw = vslot & 7;
+
+    for (int st = 0; st < n_st; ++st) {
+        const int s = st % T::kStages;
+        const uint32_t par = static_cast<uint32_t>(st / T::kStages) & 1u;
+        const bool ok = mbar_wait(full_bar + 8 * s, par, p.wait_ns);
+        if (!__all_sync(~0u, ok)) {
+            if (lane == 0)
+                atomicOr(p.flags, SDA_FLAG_TIMEOUT);
+            break;
+        }
+        const uint32_t wm = static_cast<uint32_t>(hdr[s] >> (16 * warp)) & 0xFFFFu;
+        const uint32_t stage_base = sbase + s * L::kStageBytes;
+        if (wm) {
+            // ---- S = Q K^T for this warp's 16 slots (two n8 tiles).  Thread
+            // (g, t) reads column g's token: tile i uses slot 16w + 8i + rowmap(g).
+            float sc[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
+            const int sw = rowmap(g);
+            const uint32_t row0 = stage_base + (16 * warp + sw) * 128;
+            const uint32_t row1 = row0 + 8 * 128;
+            if constexpr (FP8) {
+                // thread t: band 0 chunks t and t+4, band 1 chunk t (16 dims each)
+#pragma unroll
+                for (int c = 0; c < 3; ++c) {
+                    const int band = c == 2 ? 1 : 0;
+                    const int ch = c == 1 ? t + 4 : t;
+                    const uint32_t off = band * kBandBytes + ((ch ^ sw) << 4);
+                    const uint4 k0 = lds128(row0 + off);
+                    const uint4 k1 = lds128(row1 + off);
+                    const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
+                    const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 qv = lds128(qfrag + ((4 * c + j) * 32 + lane) * 16);
+                        const uint32_t qf[4] = {qv.x, qv.y, qv.z, qv.w};
+                        mma16816<true>(sc[0], qf, e4m3x2_to_f16x2(w0[j]), e4m3x2_to_f16x2(w0[j] >> 16));
+                        mma16816<true>(sc[1], qf, e4m3x2_to_f16x2(w1[j]), e4m3x2_to_f16x2(w1[j] >> 16));
+                    }
+                }
+            } else {
+                // thread t: bands 0-2, chunks t and t+4 (8 dims each, two k-steps)
+#pragma unroll
+                for (int j = 0; j < 6; ++j) {
+                    const int band = j >> 1;
+                    const int ch = (j & 1) * 4 + t;
+                    const uint32_t off = band * kBandBytes + ((ch ^ sw) << 4);
+                    const uint4 k0 = lds128(row0 + off);
+                    const uint4 k1 = lds128(row1 + off);
+                    const uint4 qa = lds128(qfrag + ((2 * j) * 32 + lane) * 16);
+                    const uint4 qb = lds128(qfrag + ((2 * j + 1) * 32 + lane) * 16);
+                    const uint32_t qfa[4] = {qa.x, qa.y, qa.z, qa.w};
+                    const uint32_t qfb[4] = {qb.x, qb.y, qb.z, qb.w};
+                    mma16816<false>(sc[0], qfa, k0.x, k0.y);
+                    mma16816<false>(sc[1], qfa, k1.x, k1.y);
+                    mma16816<false>(sc[0], qfb, k0.z, k0.w);
+                    mma16816<false>(sc[1], qfb, k1.z, k1.w);
+                }
+            }
+
+            // ---- Mask, online softmax.  c0/c2 are slot 8i+t, c1/c3 slot 8i+t+4.
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const bool v0 = (wm >> (8 * i + t)) & 1u;
+                const bool v1 = (wm >> (8 * i + t + 4)) & 1u;
+                sc[i][0] = v0 ? sc[i][0] * sl2 : -INFINITY;
+                sc[i][1] = v1 ? sc[i][1] * sl2 : -INFINITY;
+                sc[i][2] = v0 ? sc[i][2] * sl2 : -INFINITY;
+                sc[i][3] = v1 ? sc[i][3] * sl2 : -INFINITY;
+                mx0 = fmaxf(mx0, fmaxf(sc[i][0], sc[i][1]));
+                mx1 = fmaxf(mx1, fmaxf(sc[i][2], sc[i][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(~0u, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(~0u, mx1, 2));
+            const bool need = mx0 > m_run[0] + kRescaleSlack || mx1 > m_run[1] + kRescaleSlack;
+            if (__any_sync(~0u, need)) {
+                const float n0 = fmaxf(m_run[0], mx0), n1 = fmaxf(m_run[1], mx1);
+                const float a0 = n0 == -INFINITY ? 1.0f : fast_exp2(m_run[0] - n0);
+                const float a1 = n1 == -INFINITY ? 1.0f : fast_exp2(m_run[1] - n1);
+                m_run[0] = n0;
+                m_run[1] = n1;
+                l_run[0] *= a0;
+                l_run[1] *= a1;
+#pragma unroll
+                for (int n = 0; n < 24; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+            }
+            float pr[2][4];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                pr[i][0] = m_run[0] == -INFINITY ? 0.0f : fast_exp2(sc[i][0] - m_run[0]);
+                pr[i][1] = m_run[0] == -INFINITY ? 0.0f : fast_exp2(sc[i][1] - m_run[0]);
+                pr[i][2] = m_run[1] == -INFINITY ? 0.0f : fast_exp2(sc[i][2] - m_run[1]);
+                pr[i][3] = m_run[1] == -INFINITY ? 0.0f : fast_exp2(sc[i][3] - m_run[1]);
+            }
+            l_run[0] += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+            l_run[1] += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+            const uint32_t pa[4] = {pack2<FP8>(pr[0][0], pr[0][1]), pack2<FP8>(pr[0][2], pr[0][3]),
+                                    pack2<FP8>(pr[1][0], pr[1][1]), pack2<FP8>(pr[1][2], pr[1][3])};
+
+            // ---- O += P V.  Invalid slots' V may hold anything (even NaN):
+            // zero them when this warp's 16 slots are not all valid.
+            uint32_t vm0 = ~0u, vm1 = ~0u;
+            if (wm != 0xFFFFu) {
+                vm0 = (((wm >> t) & 1u) ? 0x0000FFFFu : 0u) | (((wm >> (t + 4)) & 1u) ? 0xFFFF0000u : 0u);
+                vm1 = (((wm >> (t + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((wm >> (t + 12)) & 1u) ? 0xFFFF0000u : 0u);
+            }
+            const uint32_t vrow = stage_base + vslot * 128;
+            if constexpr (FP8) {
+                // 16-dim chunks cv = 0..11: V dims 0..63 sit in band 1 chunks 4..7,
+                // dims 64..191 in band 2 chunks 0..7.  One chunk gives two n8
+                // tiles: even dims (2*cv) and odd dims (2*cv + 1).
+#pragma unroll
+                for (int c2 = 0; c2 < 6; ++c2) {
+                    const int cv = 2 * c2 + (mi >> 1);
+                    const int band = cv < 4 ? 1 : 2;
+                    const int ch = cv < 4 ? cv + 4 : cv - 4;
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_trans(vrow + band * kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+                    r0 &= vm0;
+                    r1 &= vm1;
+                    r2 &= vm0;
+                    r3 &= vm1;
+                    const uint32_t x0 = prmt(r0, 0x3120u), x1 = prmt(r1, 0x3120u);
+                    const uint32_t x2 = prmt(r2, 0x3120u), x3 = prmt(r3, 0x3120u);
+                    mma16816<true>(o[4 * c2 + 0], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
+                    mma16816<true>(o[4 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+                    mma16816<true>(o[4 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
+                    mma16816<true>(o[4 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
+                }
+            } else {
+                // 8-dim chunks cv = 0..23 in bands 3..5; one n8 tile each.
+#pragma unroll
+                for (int c2 = 0; c2 < 12; ++c2) {
+                    const int cv = 2 * c2 + (mi >> 1);
+                    const int band = 3 + (cv >> 3);
+                    const int ch = cv & 7;
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_trans(vrow + band * kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+                    mma16816<false>(o[2 * c2], pa, r0 & vm0, r1 & vm1);
+                    mma16816<false>(o[2 * c2 + 1], pa, r2 & vm0, r3 & vm1);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(empty_bar + 8 * s);
+    }
+
+    // ---- Epilogue: merge the four warps.
+    float l0 = l_run[0], l1 = l_run[1];
+    l0 += __shfl_xor_sync(~0u, l0, 1);
+    l0 += __shfl_xor_sync(~0u, l0, 2);
+    l1 += __shfl_xor_sync(~0u, l1, 1);
+    l1 += __shfl_xor_sync(~0u, l1, 2);
+    if (t == 0) {
+        ml[(warp * kMaxHeads + g) * 2 + 0] = m_run[0];
+        ml[(warp * kMaxHeads + g) * 2 + 1] = l0;
+        ml[(warp * kMaxHeads + g + 8) * 2 + 0] = m_run[1];
+        ml[(warp * kMaxHeads + g + 8) * 2 + 1] = l1;
+    }
+    const int ctid = threadIdx.x;          // 0..127 among consumers
+    const int64_t tok = row / p.groups;
+    const int grp = row % p.groups;
+    if (ctid < p.heads)
+        gam[ctid] = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + ctid) * p.g_s1])
+                           : 1.0f;
+    consumer_bar();
+
+    float fac[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int h = g + 8 * r;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            M = fmaxf(M, ml[(w * kMaxHeads + h) * 2]);
+        float Ls = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float mw = ml[(w * kMaxHeads + h) * 2];
+            if (mw != -INFINITY)
+                Ls += ml[(w * kMaxHeads + h) * 2 + 1] * fast_exp2(mw - M);
+        }
+        const float mine = m_run[r];
+        fac[r] = (Ls > 0.0f && mine != -INFINITY) ? fast_exp2(mine - M) / Ls : 0.0f;
+        if (p.splits > 1 && warp == 0 && t == 0 && h < p.heads && act)
+            p.lse[(static_cast<int64_t>(row) * p.splits + split) * p.heads + h] =
+                Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    }
+
+    // Scaled per-warp outputs into the (now idle) stage ring.
+    float *obuf = reinterpret_cast<float *>(smem);
+    float *ob0 = obuf + (warp * kMaxHeads + g) * kObufStride;
+    float *ob1 = obuf + (warp * kMaxHeads + g + 8) * kObufStride;
+    if constexpr (FP8) {
+#pragma unroll
+        for (int cv = 0; cv < 12; ++cv) {
+            const int d = 16 * cv + 4 * t;
+            *reinterpret_cast<float4 *>(ob0 + d) =
+                make_float4(o[2 * cv][0] * fac[0], o[2 * cv + 1][0] * fac[0], o[2 * cv][1] * fac[0],
+                            o[2 * cv + 1][1] * fac[0]);
+            *reinterpret_cast<float4 *>(ob1 + d) =
+                make_float4(o[2 * cv][2] * fac[1], o[2 * cv + 1][2] * fac[1], o[2 * cv][3] * fac[1],
+                            o[2 * cv + 1][3] * fac[1]);
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < 24; ++n) {
+            const int d = 8 * n + 2 * t;
+            *reinterpret_cast<float2 *>(ob0 + d) = make_float2(o[n][0] * fac[0], o[n][1] * fac[0]);
+            *reinterpret_cast<float2 *>(ob1 + d) = make_float2(o[n][2] * fac[1], o[n][3] * fac[1]);
+        }
+    }
+    consumer_bar();
+
+    const int total = p.heads * kDim;
+    if (p.splits == 1) {
+        if (!act && !p.clear_inactive)
+            return;
+        uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0;
+        for (int e = ctid; e < total; e += kConsumerWarps * 32) {
+            const int h = e / kDim, d = e - h * kDim;
+            float v = 0.0f;
+            if (act) {
+                v = obuf[h * kObufStride + d] + obuf[(kMaxHeads + h) * kObufStride + d] +
+                    obuf[(2 * kMaxHeads + h) * kObufStride + d] + obuf[(3 * kMaxHeads + h) * kObufStride + d];
+                v = v * vfold * gam[h];
+            }
+            out[static_cast<int64_t>(h) * p.o_s1 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+    } else if (act) {
+        float *dst = p.partial + (static_cast<int64_t>(row) * p.splits + split) * p.heads * kDim;
+        for (int e = ctid; e < total; e += kConsumerWarps * 32) {
+            const int h = e / kDim, d = e - h * kDim;
+            const float v = obuf[h * kObufStride + d] + obuf[(kMaxHeads + h) * kObufStride + d] +
+                            obuf[(2 * kMaxHeads + h) * kObufStride + d] +
+                            obuf[(3 * kMaxHeads + h) * kObufStride + d];
+            dst[e] = v * vfold;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Combine kernel: one CTA per row merges the splits through their LSEs,
+// applies the gate and clears inactive rows.
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(128) sda_combine_kernel(const __grid_constant__ Params p)
+{
+    __shared__ float wts[kMaxHeads][kMaxSplits];
+    __shared__ float gam[kMaxHeads];
+    pdl_wait();   // partials come from the split kernel
+    const int row = blockIdx.x;
+    const bool act = p.active[row * p.act_s0] != 0;
+    uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0;
+    const int total = p.heads * kDim;
+    if (!act) {
+        if (p.clear_inactive)
+            for (int e = threadIdx.x; e < total; e += blockDim.x) {
+                const int h = e / kDim, d = e - h * kDim;
+                out[static_cast<int64_t>(h) * p.o_s1 + d] = 0;
+            }
+        return;
+    }
+    if (threadIdx.x < p.heads) {
+        const int h = threadIdx.x;
+        const float *l = p.lse + static_cast<int64_t>(row) * p.splits * p.heads + h;
+        float M = -INFINITY;
+        for (int s = 0; s < p.splits; ++s)
+            M = fmaxf(M, l[s * p.heads]);
+        float sum = 0.0f;
+        for (int s = 0; s < p.splits; ++s) {
+            const float w = M == -INFINITY ? 0.0f : expf(l[s * p.heads] - M);
+            wts[h][s] = w;
+            sum += w;
+        }
+        const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
+        for (int s = 0; s < p.splits; ++s)
+            wts[h][s] *= inv;
+        const int64_t tok = row / p.groups;
+        const int grp = row % p.groups;
+        gam[h] = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
+                        : 1.0f;
+    }
+    __syncthreads();
+    const float *part = p.partial + static_cast<int64_t>(row) * p.splits * p.heads * kDim;
+    for (int e = threadIdx.x; e < total; e += blockDim.x) {
+        const int h = e / kDim, d = e - h * kDim;
+        float v = 0.0f;
+        for (int s = 0; s < p.splits; ++s)
+            v += wts[h][s] * part[(static_cast<int64_t>(s) * p.heads + h) * kDim + d];
+        out[static_cast<int64_t>(h) * p.o_s1 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v * gam[h]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+std::atomic<unsigned long long> g_wait_ns{1000000000ull};
+
+bool dims_ok(const sda_tensor *t, int ndim)
+{
+    if (!t || t->ndim != ndim)
+        return false;
+    for (int i = 0; i < ndim; ++i)
+        if (t->shape[i] < 0)
+            return false;
+    return true;
+}
+
+// The dynamic shared memory limit each kernel instantiation has been raised to,
+// per device.
+template <bool FP8>
+cudaError_t ensure_smem(size_t bytes)
+{
+    static std::mutex mu;
+    static size_t raised[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t &cur = raised[dev & 63];
+    if (bytes <= cur)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(sda_split_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(bytes));
+    if (e == cudaSuccess)
+        cur = bytes;
+    return e;
+}
+
+template <bool FP8>
+sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, cudaStream_t stream)
+{
+    const size_t smem = Layout<FP8>::bytes(num_regions);
+    if (smem > 227 * 1024)
+        return SDA_ERR_UNSUPPORTED;
+    if (ensure_smem<FP8>(smem) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(prm.rows) * static_cast<unsigned>(prm.splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8>, tmap, prm) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    if (prm.splits > 1) {
+        cudaLaunchConfig_t c2 = {};
+        c2.gridDim = dim3(static_cast<unsigned>(prm.rows));
+        c2.blockDim = dim3(128);
+        c2.dynamicSmemBytes = 0;
+        c2.stream = stream;
+        c2.attrs = attr;
+        c2.numAttrs = 1;
+        if (cudaLaunchKernelEx(&c2, sda_combine_kernel, prm) != cudaSuccess)
+            return SDA_ERR_CUDA;
+    }
+    return SDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_decode_splits(int rows)
+{
+    int splits = 1;
+    while (splits < 32 && static_cast<long long>(rows) * splits * 2 <= 256)
+        splits *= 2;
+    return rows < 0 ? 1 : splits;
+}
+
+size_t sparse_decode_workspace_bytes(int rows, int heads, int splits)
+{
+    if (rows < 0 || heads < 1 || heads > kMaxHeads || splits < 1 || splits > kMaxSplits)
+        return 0;
+    size_t bytes = kHeaderBytes;
+    if (splits > 1) {
+        const size_t n = static_cast<size_t>(rows) * splits * heads;
+        bytes += n * kDim * sizeof(float);
+        bytes += (n * sizeof(float) + 255) & ~static_cast<size_t>(255);
+    }
+    return bytes;
+}
+
+void sparse_decode_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_ns.store(ns);
+}
+
+const char *sparse_decode_status_string(int status)
+{
+    switch (status) {
+    case SDA_OK: return "ok";
+    case SDA_ERR_INVALID: return "invalid argument";
+    case SDA_ERR_UNSUPPORTED: return "unsupported argument combination";
+    case SDA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SDA_ERR_CUDA: return "CUDA call failed";
+    case SDA_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case SDA_ERR_BOUNDS: return "an index read from the inputs was out of range";
+    default: return "unknown status";
+    }
+}
+
+sda_status sparse_decode_read_errors(const void *workspace, uint32_t *flags, int clear, void *stream)
+{
+    if (!workspace || !flags)
+        return SDA_ERR_INVALID;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t host = 0;
+    if (cudaMemcpyAsync(&host, workspace, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    *flags = host;
+    if (clear) {
+        if (cudaMemsetAsync(const_cast<void *>(workspace), 0, sizeof host, s) != cudaSuccess)
+            return SDA_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess)
+            return SDA_ERR_CUDA;
+    }
+    return SDA_OK;
+}
+
+sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *cache,
+                                   const sda_tensor *regions, const sda_tensor *block_table,
+                                   const sda_tensor *positions, const sda_tensor *active,
+                                   const sda_tensor *output, float scale, int query_len,
+                                   int splits, const float *k_scale, const float *v_scale,
+                                   const sda_tensor *gate, int clear_inactive, int region_tokens,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    // ---- Shape / dtype / stride contract (the page's asserts and the
+    // eligibility test of the direct sparse decode path).
+    if (!dims_ok(query, 3) || !dims_ok(cache, 4) || !dims_ok(regions, 2) || !dims_ok(block_table, 2) ||
+        !dims_ok(positions, 1) || !dims_ok(active, 1) || !dims_ok(output, 3))
+        return SDA_ERR_INVALID;
+    const int64_t rows = query->shape[0], heads = query->shape[1];
+    if (query->dtype != SDA_DTYPE_BF16 || output->dtype != SDA_DTYPE_BF16)
+        return SDA_ERR_INVALID;
+    if (query->shape[2] != kDim || cache->shape[3] != kRow)
+        return SDA_ERR_INVALID;
+    if (heads < 1 || heads > kMaxHeads)
+        return SDA_ERR_UNSUPPORTED;
+    if (output->shape[0] != rows || output->shape[1] != heads || output->shape[2] != kDim)
+        return SDA_ERR_INVALID;
+    if (query->stride[2] != 1 || output->stride[2] != 1 || cache->stride[3] != 1)
+        return SDA_ERR_INVALID;
+    if (regions->dtype != SDA_DTYPE_INT32 || regions->shape[0] != rows || regions->stride[1] != 1)
+        return SDA_ERR_INVALID;
+    if (block_table->dtype != SDA_DTYPE_INT32 || block_table->stride[1] != 1)
+        return SDA_ERR_INVALID;
+    if (positions->dtype != SDA_DTYPE_INT32 || positions->shape[0] != rows)
+        return SDA_ERR_INVALID;
+    if ((active->dtype != SDA_DTYPE_BOOL && active->dtype != SDA_DTYPE_UINT8) || active->shape[0] != rows)
+        return SDA_ERR_INVALID;
+    const bool fp8 = cache->dtype == SDA_DTYPE_FP8_E4M3 || cache->dtype == SDA_DTYPE_UINT8;
+    if (!fp8 && cache->dtype != SDA_DTYPE_BF16)
+        return SDA_ERR_INVALID;
+    if (fp8 && (!k_scale || !v_scale))
+        return SDA_ERR_INVALID;
+    if (query_len < 1 || splits < 1 || splits > kMaxSplits || !std::isfinite(scale))
+        return SDA_ERR_INVALID;
+    const int64_t pages = cache->shape[0], groups = cache->shape[1], block = cache->shape[2];
+    if (groups < 1 || block < 1 || pages < 1 || pages > INT32_MAX)
+        return SDA_ERR_INVALID;
+    if (rows % groups != 0)
+        return SDA_ERR_INVALID;
+    const int64_t per_req = groups * query_len;
+    if (rows > 0 && (rows + per_req - 1) / per_req > block_table->shape[0])
+        return SDA_ERR_INVALID;
+    const bool gated = gate && gate->data;
+    if (gated) {
+        if (!dims_ok(gate, 2) || gate->dtype != SDA_DTYPE_BF16 || gate->shape[0] != rows / groups ||
+            gate->shape[1] != groups * heads)
+            return SDA_ERR_INVALID;
+    }
+    const int64_t rt = region_tokens == 0 ? block : region_tokens;
+    if (rt < 1 || rt > (1 << 24))
+        return SDA_ERR_INVALID;
+    const int64_t piece = std::min<int64_t>(std::min<int64_t>(rt, block), kSlots);
+    if (piece % 8 != 0 || rt % piece != 0 || block % piece != 0)
+        return SDA_ERR_UNSUPPORTED;
+    if (regions->shape[1] > (1 << 14) || block_table->shape[1] > INT32_MAX)
+        return SDA_ERR_UNSUPPORTED;
+    if (rows > INT32_MAX / kMaxSplits)
+        return SDA_ERR_UNSUPPORTED;
+    // TMA: 16-byte aligned base and byte strides.
+    const int elt = fp8 ? 1 : 2;
+    const uintptr_t cbase = reinterpret_cast<uintptr_t>(cache->data);
+    if (cbase % 16 != 0 || (cache->stride[0] * elt) % 16 != 0 || (cache->stride[1] * elt) % 16 != 0 ||
+        (cache->stride[2] * elt) % 16 != 0 || cache->stride[0] <= 0 || cache->stride[1] <= 0 ||
+        cache->stride[2] <= 0)
+        return SDA_ERR_UNSUPPORTED;
+    const size_t need = sparse_decode_workspace_bytes(static_cast<int>(rows), static_cast<int>(heads), splits);
+    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < need)
+        return SDA_ERR_WORKSPACE;
+    if (rows == 0)
+        return SDA_OK;
+    if (!query->data || !cache->data || !regions->data || !block_table->data || !positions->data ||
+        !active->data || !output->data)
+        return SDA_ERR_INVALID;
+
+    // ---- Tensor map over the whole cache: dims (384, B, G, pages), boxes of
+    // 128 bytes x P tokens, 128-byte swizzle.
+    EncodeTiledFn encode = encode_fn();
+    if (!encode)
+        return SDA_ERR_CUDA;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(block),
+                                static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(pages)};
+    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(cache->stride[2] * elt),
+                                   static_cast<cuuint64_t>(cache->stride[1] * elt),
+                                   static_cast<cuuint64_t>(cache->stride[0] * elt)};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(piece), 1, 1};
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    if (encode(&tmap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<void *>(cache->data), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SDA_ERR_UNSUPPORTED;
+
+    Params prm;
+    std::memset(&prm, 0, sizeof prm);
+    prm.query = static_cast<const uint16_t *>(query->data);
+    prm.q_s0 = query->stride[0];
+    prm.q_s1 = query->stride[1];
+    prm.regions = static_cast<const int32_t *>(regions->data);
+    prm.reg_s0 = regions->stride[0];
+    prm.block_table = static_cast<const int32_t *>(block_table->data);
+    prm.bt_s0 = block_table->stride[0];
+    prm.positions = static_cast<const int32_t *>(positions->data);
+    prm.pos_s0 = positions->stride[0];
+    prm.active = static_cast<const uint8_t *>(active->data);
+    prm.act_s0 = active->stride[0];
+    prm.output = static_cast<uint16_t *>(const_cast<void *>(output->data));
+    prm.o_s0 = output->stride[0];
+    prm.o_s1 = output->stride[1];
+    prm.gate = gated ? static_cast<const uint16_t *>(gate->data) : nullptr;
+    prm.g_s0 = gated ? gate->stride[0] : 0;
+    prm.g_s1 = gated ? gate->stride[1] : 0;
+    prm.k_scale = k_scale;
+    prm.v_scale = v_scale;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.flags = reinterpret_cast<unsigned int *>(ws);
+    if (splits > 1) {
+        const size_t n = static_cast<size_t>(rows) * splits * heads;
+        prm.partial = reinterpret_cast<float *>(ws + kHeaderBytes);
+        prm.lse = reinterpret_cast<float *>(ws + kHeaderBytes + n * kDim * sizeof(float));
+    }
+    prm.pages = pages;
+    prm.wait_ns = g_wait_ns.load();
+    prm.scale = scale;
+    prm.num_regions = static_cast<int>(regions->shape[1]);
+    prm.table_cols = static_cast<int>(block_table->shape[1]);
+    prm.rows = static_cast<int>(rows);
+    prm.heads = static_cast<int>(heads);
+    prm.groups = static_cast<int>(groups);
+    prm.block = static_cast<int>(block);
+    prm.region_tokens = static_cast<int>(rt);
+    prm.piece = static_cast<int>(piece);
+    prm.query_len = query_len;
+    prm.splits = splits;
+    prm.clear_inactive = clear_inactive ? 1 : 0;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return fp8 ? launch<true>(tmap, prm, prm.num_regions, s) : launch<false>(tmap, prm, prm.num_regions, s);
+}
+
+}  // extern "C"

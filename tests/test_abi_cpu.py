@@ -1,0 +1,155 @@
+"""Host-side tests of the C-ABI library (no GPU needed).
+
+The library loads and exports every entry point include/sdattn.h declares;
+the split policy and workspace sizing are exact; every contract violation is
+rejected with its status code before any CUDA call is made."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_decode_attention_02_gb300 as sda
+from sparse_decode_attention_02_gb300 import _binding as B
+from sparse_decode_attention_02_gb300 import build as lib_build
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return sda.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = sda.declared_functions()
+    assert {"sparse_decode_attention", "sparse_decode_splits", "sparse_decode_workspace_bytes",
+            "sparse_decode_read_errors"} <= set(names)
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_splits_truth_table(lib):
+    with open(os.path.join(GOLDEN, "sparse_decode_splits.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            lo, hi, s = (int(x) for x in line.split())
+            for rows in range(lo, hi + 1):
+                assert sda.sparse_decode_splits(rows) == s, rows
+    assert sda.sparse_decode_splits(10 ** 6) == 1
+
+
+def test_workspace_bytes(lib):
+    assert sda.workspace_bytes(100, 16, 1) == 256
+    n = 128 * 2 * 16
+    assert sda.workspace_bytes(128, 16, 2) == 256 + n * 192 * 4 + ((n * 4 + 255) // 256) * 256
+    assert sda.workspace_bytes(4, 17, 1) == 0
+    assert sda.workspace_bytes(4, 8, 65) == 0
+
+
+class FakeDev:
+    """Descriptors with fake device addresses: validation never dereferences them."""
+
+    def __init__(self, rows=8, H=16, pages=64, G=2, Bk=64, R=8, reqs=4, W=16, fp8=False):
+        self.rows, self.H = rows, H
+        self.q = self.t(1, (rows, H, 192))
+        self.cache = self.t(3 if fp8 else 1, (pages, G, Bk, 384))
+        self.regions = self.t(4, (rows, R))
+        self.table = self.t(4, (reqs, W))
+        self.pos = self.t(4, (rows,))
+        self.act = self.t(5, (rows,))
+        self.out = self.t(1, (rows, H, 192))
+        self.gate = None
+        self.fp8 = fp8
+
+    @staticmethod
+    def t(dtype, shape, strides=None, addr=1 << 20):
+        d = B.SdaTensor()
+        d.data = addr
+        d.dtype = dtype
+        d.ndim = len(shape)
+        if strides is None:
+            strides, acc = [], 1
+            for n in reversed(shape):
+                strides.insert(0, acc)
+                acc *= n
+        for i, (n, s) in enumerate(zip(shape, strides)):
+            d.shape[i] = n
+            d.stride[i] = s
+        return d
+
+    def call(self, lib, splits=1, rt=0, ws_bytes=None, ws_addr=1 << 24, query_len=1, scale=0.07,
+             kscale=True):
+        ws_bytes = lib.sparse_decode_workspace_bytes(self.rows, self.H, splits) if ws_bytes is None else ws_bytes
+        ks = ctypes.c_void_p(1 << 12) if (self.fp8 and kscale) else None
+        r = ctypes.byref
+        return lib.sparse_decode_attention(
+            r(self.q), r(self.cache), r(self.regions), r(self.table), r(self.pos), r(self.act),
+            r(self.out), scale, query_len, splits, ks, ks,
+            r(self.gate) if self.gate is not None else None, 1, rt, ws_addr, ws_bytes, None)
+
+
+def test_rejects_contract_violations(lib):
+    INV, UNS, WS = B.SDA_ERR_INVALID, B.SDA_ERR_UNSUPPORTED, B.SDA_ERR_WORKSPACE
+    f = FakeDev(H=17)
+    f.q = f.t(1, (8, 17, 192)); f.out = f.t(1, (8, 17, 192))
+    assert f.call(lib) == UNS                                   # heads > 16
+    f = FakeDev(); f.q = f.t(1, (8, 16, 191)); assert f.call(lib) == INV     # dim != 192
+    f = FakeDev(); f.cache = f.t(1, (64, 2, 64, 383)); assert f.call(lib) == INV
+    f = FakeDev(); f.q = f.t(1, (8, 16, 192), (16 * 384, 384, 2)); assert f.call(lib) == INV  # inner stride
+    f = FakeDev(); f.regions = f.t(4, (8, 8), (16, 2)); assert f.call(lib) == INV
+    f = FakeDev(); f.regions = f.t(4, (7, 8)); assert f.call(lib) == INV      # rows mismatch
+    f = FakeDev(); f.pos = f.t(1, (8,)); assert f.call(lib) == INV            # dtype
+    f = FakeDev(fp8=True); assert f.call(lib, kscale=False) == INV            # FP8 without scales
+    f = FakeDev(); assert f.call(lib, splits=0) == INV
+    f = FakeDev(); assert f.call(lib, splits=65) == INV
+    f = FakeDev(); assert f.call(lib, query_len=0) == INV
+    f = FakeDev(); assert f.call(lib, scale=float("nan")) == INV
+    f = FakeDev(rows=7); f.regions = f.t(4, (7, 8)); f.pos = f.t(4, (7,)); f.act = f.t(5, (7,))
+    f.q = f.t(1, (7, 16, 192)); f.out = f.t(1, (7, 16, 192))
+    assert f.call(lib) == INV                                   # rows not a multiple of G
+    f = FakeDev(rows=12, reqs=2)
+    for name in ("regions", "pos", "act"):
+        pass
+    f.regions = f.t(4, (12, 8)); f.pos = f.t(4, (12,)); f.act = f.t(5, (12,))
+    f.q = f.t(1, (12, 16, 192)); f.out = f.t(1, (12, 16, 192))
+    assert f.call(lib) == INV                                   # more requests than table rows
+    f = FakeDev(); f.gate = f.t(1, (4, 31)); assert f.call(lib) == INV       # gate width != G*H
+    f = FakeDev(); assert f.call(lib, rt=4) == UNS             # piece not a multiple of 8
+    f = FakeDev(); assert f.call(lib, rt=24) == UNS            # RT not a multiple of the piece
+    f = FakeDev(); f.cache = f.t(1, (64, 2, 64, 384), (2 * 64 * 384 + 3, 64 * 384, 384, 1))
+    assert f.call(lib) == UNS                                   # page stride not 16-byte
+    f = FakeDev(); assert f.call(lib, ws_bytes=100) == WS
+    f = FakeDev(); assert f.call(lib, ws_addr=(1 << 24) + 16) == WS         # misaligned
+    f = FakeDev(); assert f.call(lib, splits=2, ws_bytes=256) == WS
+    f = FakeDev(rows=0); f.regions = f.t(4, (0, 8)); f.pos = f.t(4, (0,)); f.act = f.t(5, (0,))
+    f.q = f.t(1, (0, 16, 192)); f.out = f.t(1, (0, 16, 192))
+    assert f.call(lib) == B.SDA_OK                              # no rows: nothing to do
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert sda.status_string(code)
+    assert "unknown" in sda.status_string(99)
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The package never imports the oracle, and a missing library raises."""
+    import sys
+    src_dir = os.path.dirname(sda.__file__)
+    for name in os.listdir(src_dir):
+        if name.endswith(".py"):
+            text = open(os.path.join(src_dir, name)).read()
+            assert "import oracle" not in text and "from oracle" not in text, name
+    saved = B._lib, B.LIB_PATH
+    try:
+        B._lib, B.LIB_PATH = None, "/nonexistent/libsdattn.so"
+        with pytest.raises(ImportError):
+            B.load()
+    finally:
+        B._lib, B.LIB_PATH = saved
