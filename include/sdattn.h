@@ -154,6 +154,40 @@ sda_status sparse_decode_read_errors(const void *workspace, uint32_t *flags, int
  */
 void sparse_decode_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Allocation-free variant of sparse_decode_attention.  The page has no
+ * counterpart for it.
+ *
+ * For callers that cannot obtain device memory for a workspace: plugin or
+ * FFI hosts that are handed tensor pointers by another runtime but no
+ * allocator, and code running where a cudaMalloc would synchronise the device
+ * or break a stream capture in progress.  Arguments and results are those of
+ * sparse_decode_attention without `workspace` / `workspace_bytes`: the
+ * scratch (flag header, split partials and LSEs) lives in an 8 MiB static
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.
+ *   - Limit: sparse_decode_workspace_bytes(rows, H, splits) must be at most
+ *     8 MiB (8388608), else SDA_ERR_WORKSPACE is returned and nothing is
+ *     enqueued.  splits == 1 needs 256 bytes, so any row count fits; with
+ *     16 heads, rows * splits up to 679 fits.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the previous
+ *     call's contents.  Calls whose kernels overlap on the GPU (different
+ *     streams, no ordering between them) race on it: serialise them.
+ *   - Each call clears the flag header (an async memset on `stream`); device
+ *     flags of this variant are not reported to the caller.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ */
+sda_status sparse_decode_attention_no_alloc(const sda_tensor *query, const sda_tensor *cache,
+                                            const sda_tensor *regions, const sda_tensor *block_table,
+                                            const sda_tensor *positions, const sda_tensor *active,
+                                            const sda_tensor *output, float scale, int query_len,
+                                            int splits, const float *k_scale, const float *v_scale,
+                                            const sda_tensor *gate, int clear_inactive,
+                                            int region_tokens, void *stream);
+
 /* A static description of a status code. */
 const char *sparse_decode_status_string(int status);
 

@@ -188,3 +188,36 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def status_string(code: int) -> str:
     return load().sparse_decode_status_string(int(code)).decode()
+
+
+def sparse_decode_attention_no_alloc(query, cache, regions, block_table, positions, active, output, *,
+                                     scale: float, query_len: int = 1, splits: int | None = None,
+                                     clear_inactive: bool = True, k_scale=None, v_scale=None, gate=None,
+                                     region_tokens: int = 0, stream: torch.cuda.Stream | None = None) -> None:
+    """The allocation-free C entry point: same contract as sparse_decode_attention
+    but its scratch is the library's static 8 MiB device array (no workspace
+    argument).  For callers that cannot allocate device memory; calls that
+    overlap on the GPU race on the shared array.  `k_scale`/`v_scale` must be
+    device tensors here (uploading a python float would allocate)."""
+    lib = load()
+    fn = lib.sparse_decode_attention_no_alloc
+    if not fn.argtypes:
+        P = ctypes.POINTER(SdaTensor)
+        fn.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                       ctypes.c_void_p, P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    rows = query.shape[0]
+    if splits is None:
+        splits = lib.sparse_decode_splits(rows)
+    for x in (k_scale, v_scale):
+        if x is not None and not isinstance(x, torch.Tensor):
+            raise TypeError("k_scale / v_scale must be device tensors for the allocation-free call")
+    ks = k_scale.data_ptr() if k_scale is not None else None
+    vs = v_scale.data_ptr() if v_scale is not None else None
+    descs = [describe(x) for x in (query, cache, regions, block_table, positions, active, output)]
+    gd = describe(gate)
+    s = stream if stream is not None else torch.cuda.current_stream(query.device)
+    rc = fn(*[_ref(d) for d in descs], float(scale), int(query_len), int(splits), ks, vs, _ref(gd),
+            int(bool(clear_inactive)), int(region_tokens), s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())

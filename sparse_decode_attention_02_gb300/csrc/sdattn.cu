@@ -1124,3 +1124,65 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// For callers that hold device pointers to their tensors but have no way to
+// obtain more device memory: plugin or FFI hosts that receive buffers from
+// another runtime without an allocator handle, and code running where a
+// cudaMalloc would synchronise the device or break a stream capture in
+// progress.  The split-KV scratch (flag header, fp32 partials and LSEs) lives
+// in the fixed file-scope array below instead of a caller-supplied buffer.
+// Every GPU that loads this library holds the array until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+static __device__ __align__(256) unsigned char g_sda_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_scratch_mu;
+void *g_static_scratch_ptr[256] = {};   // device address of the array, per device
+
+}  // namespace
+
+extern "C" sda_status sparse_decode_attention_no_alloc(
+    const sda_tensor *query, const sda_tensor *cache, const sda_tensor *regions,
+    const sda_tensor *block_table, const sda_tensor *positions, const sda_tensor *active,
+    const sda_tensor *output, float scale, int query_len, int splits, const float *k_scale,
+    const float *v_scale, const sda_tensor *gate, int clear_inactive, int region_tokens, void *stream)
+{
+    if (!query || query->ndim != 3)
+        return SDA_ERR_INVALID;
+    // Size check first: the shared array must hold this call's scratch.
+    const size_t need = sparse_decode_workspace_bytes(static_cast<int>(query->shape[0]),
+                                                      static_cast<int>(query->shape[1]), splits);
+    if (query->shape[0] < 0 || query->shape[0] > INT32_MAX || need == 0 || need > kStaticScratchBytes)
+        return SDA_ERR_WORKSPACE;
+    // Once per device, with that device current: the array's device address.
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    if (dev < 0 || dev >= 256)
+        return SDA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+        if (!g_static_scratch_ptr[dev]) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_sda_static_scratch) != cudaSuccess || !p)
+                return SDA_ERR_CUDA;
+            g_static_scratch_ptr[dev] = p;
+        }
+        scratch = g_static_scratch_ptr[dev];
+    }
+    // The array keeps the previous call's contents: the kernels only OR into
+    // the flag header, so it starts every call at zero.  Partials and LSEs are
+    // written before they are read and need no clearing.
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (query->shape[0] > 0 && cudaMemsetAsync(scratch, 0, kHeaderBytes, s) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    return sparse_decode_attention(query, cache, regions, block_table, positions, active, output, scale,
+                                   query_len, splits, k_scale, v_scale, gate, clear_inactive,
+                                   region_tokens, scratch, kStaticScratchBytes, stream);
+}
