@@ -51,6 +51,16 @@ def parse():
     return ap.parse_args()
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The maximum of x over all ranks (x itself without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -170,6 +180,27 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def ncu_traffic(cfg_name, alg_bytes):
+    """Per-launch DRAM bytes from the committed ncu capture, scaled by algorithmic
+    bytes to this launch; None if the capture is for another workload or the
+    kernel source changed since it was taken."""
+    import hashlib
+    try:
+        fields = {}
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")) as f:
+            for line in f:
+                line = line.split("#")[0].split()
+                if len(line) == 2:
+                    fields[line[0]] = line[1]
+        src = os.path.join(ROOT, "sparse_decode_attention_02_gb300", "csrc", "sdattn.cu")
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != fields["kernel_source_sha256_16"] or fields["workload"] != cfg_name:
+            return None
+        return int(fields["dram_bytes"]) * alg_bytes / int(fields["algorithmic_bytes"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def cpu_baseline(w, n_rows, seed=0):
     """The float64 oracle on a bounded sample of the workload's rows."""
     import oracle
@@ -286,11 +317,7 @@ def main():
     kernel_ms = sum(per_launch)
     region_ms = t_start.elapsed_time(t_end)
     timed_ms = kernel_ms if flush else region_ms
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([timed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        timed_ms = float(t.item())
+    timed_ms = max_over_ranks(timed_ms, dev)            # slowest replica sets the job time
     flags = sda.read_errors(ws)
 
     total_rows = w.rows * steps * world
@@ -313,7 +340,8 @@ def main():
         "selected_kv_frac_of_peak": kv_gbs / world / peak,
         "active_rows_per_s": value * float((w.active.cpu().numpy() != 0).mean()),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "frac": achieved / peak, "traffic": ncu_traffic(cfg.name, alg_bytes),
+                     "peak_kind": peak_kind,
                      "kernel": "sda_split_kernel" + (" + sda_combine_kernel" if splits > 1 else ""),
                      "algorithmic_bytes_per_launch": alg_bytes, "avg_launch_ms": avg_launch_ms},
         "gpu_launches": steps * (2 if splits > 1 else 1),
