@@ -349,6 +349,42 @@ def main():
         "clocks": clocks.summary(),
     }
 
+    # ---- the same step replayed from a CUDA graph (no host launch work per step)
+    graph_steps = max(20, steps // 4)
+    try:
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+
+        def gstep():
+            sda.sparse_decode_attention(w.query, w.cache, w.regions, w.block_table, w.positions,
+                                        w.active, out, scale=w.scale, query_len=w.query_len,
+                                        splits=splits, k_scale=ks, v_scale=vs, gate=w.gate,
+                                        region_tokens=w.region_tokens, workspace=ws, stream=gstream)
+
+        with torch.cuda.stream(gstream):
+            gstep()
+            gstream.synchronize()
+            with torch.cuda.graph(graph, stream=gstream):
+                gstep()
+        g_ms = []
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        for _ in range(graph_steps):
+            if flush:
+                scratch.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            g_ms.append((a, b))
+        torch.cuda.synchronize()
+        line["graph_ms_per_step"] = statistics.median(x.elapsed_time(y) for x, y in g_ms)
+    except RuntimeError as e:                      # reported, never fatal to the bench line
+        line["graph_ms_per_step"] = None
+        line["graph_error"] = str(e)[:200]
+
     # ---- end to end through the public API: pinned host inputs -> device, call, output -> host
     if not args.no_e2e:
         host = {k: v.cpu().pin_memory() for k, v in dict(q=w.query, reg=w.regions, bt=w.block_table,

@@ -55,6 +55,10 @@ def _declare(lib):
     lib.oracle_sparse_decode_attention.restype = i32
     lib.oracle_split_partials.argtypes = common + [i32, vp, i32, vp, vp]
     lib.oracle_split_partials.restype = i32
+    lib.oracle_swa_decode.argtypes = [vp, i64, i64, i32, i32, vp, i32, i64, i32, i32, i64, i64, i64,
+                                      vp, i64, i32, i32, vp, i32, dbl, i32, i32, dbl, dbl,
+                                      vp, i64, i64, vp, i32, vp]
+    lib.oracle_swa_decode.restype = i32
     lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_decode.restype = dbl
     lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
@@ -217,6 +221,45 @@ def split_partials(query, cache, regions, block_table, positions, active, *, sca
     if rc:
         raise OracleError(_ERRORS.get(rc, str(rc)))
     return partial, lse
+
+
+def swa_decode(query, cache, block_table, seq_lens, *, scale, window, query_len=1, k_scale=None,
+               v_scale=None, gate=None, cache_fp8=None, row_ids=None, lib=None) -> np.ndarray:
+    """Gated sliding-window decode: float64 output [n, heads, 192] for ``row_ids``.
+
+    Token j of request q sits at seq_lens[q] - query_len + j and attends over the
+    ``window`` tokens ending at it (the non-DSA layers' fused decode)."""
+    lib = lib or load()
+    q = _np(query, np.uint16)
+    if cache_fp8 is None:
+        cache_fp8 = _itemsize(cache) == 1
+    c = _np(cache, np.uint8 if cache_fp8 else np.uint16)
+    bt = _np(block_table, np.int32)
+    sl = np.ascontiguousarray(_np(seq_lens, np.int32))
+    rows, heads, dim = q.shape
+    pages, groups, block, width = c.shape
+    if dim != 192 or width != 384:
+        raise ValueError("query dim must be 192 and cache rows 384 wide")
+    if cache_fp8 and (k_scale is None or v_scale is None):
+        raise ValueError("an FP8 cache needs k_scale and v_scale")
+    qs, cs, bs = _estrides(q), _estrides(c), _estrides(bt)
+    ids, n = _rows_arg(row_ids, rows)
+    out = np.zeros((n, heads, 192), dtype=np.float64)
+    if gate is not None:
+        g = _np(gate, np.uint16)
+        gs = _estrides(g)
+        gate_args = [g.ctypes.data, gs[0], gs[1]]
+    else:
+        gate_args = [None, 0, 0]
+    rc = lib.oracle_swa_decode(
+        q.ctypes.data, qs[0], qs[1], rows, heads, c.ctypes.data, int(bool(cache_fp8)), pages, groups,
+        block, cs[0], cs[1], cs[2], bt.ctypes.data, bs[0], bt.shape[0], bt.shape[1], sl.ctypes.data,
+        len(sl), float(scale), int(query_len), int(window),
+        float(k_scale if k_scale is not None else 1.0), float(v_scale if v_scale is not None else 1.0),
+        *gate_args, ids.ctypes.data if ids is not None else None, n, out.ctypes.data)
+    if rc:
+        raise OracleError(_ERRORS.get(rc, str(rc)))
+    return out
 
 
 def e4m3_decode(code: int, lib=None) -> float:

@@ -17,7 +17,11 @@
  *     of one request share one block_table row;
  *   - `_gate`: sigmoid computed in fp32 as 1 / (1 + exp(-g)), rounded to the
  *     gate's dtype (bf16) and read back as fp32;
- *   - `sparse_decode_splits`: the split-count policy.
+ *   - `sparse_decode_splits`: the split-count policy;
+ * and of the page "vllm.models.step5.nvidia.sparse_attention"
+ * (`Step5SplitKVFlashAttentionImpl.forward_with_headwise_gate`, which calls
+ * the fused gated sliding-window decode `swa_decode_gated` for the non-DSA
+ * layers with window = sliding_window[0] + 1 over the same packed cache).
  * The attention itself is the plain definition: gather the selected regions'
  * tokens, drop tokens past the row's position, softmax(scale * q k^T) v.
  *
@@ -30,7 +34,9 @@
  *   - FP8 values are decode(byte) * per-tensor scale (E4M3 "fn" encoding);
  *   - splits partition the row's compacted list of live regions (ids != -1
  *     whose first token is visible, in their stored order) into contiguous
- *     chunks [floor(s*n/S), floor((s+1)*n/S)).
+ *     chunks [floor(s*n/S), floor((s+1)*n/S));
+ *   - sliding window: token j of request q sits at p = seq_lens[q] -
+ *     query_len + j and sees the `window` tokens [max(0, p - window + 1), p].
  *
  * Everything is float64 except the gate, whose fp32 sigmoid and bf16 rounding
  * are a quantisation the page fixes in those precisions.
@@ -466,6 +472,81 @@ int oracle_split_partials(
             e = n < 0 ? (int)n : attend(&p, row, tok, n, partial + base * ORACLE_DIM, lse + base);
         }
         free(tok);
+        if (e) {
+#pragma omp critical
+            if (!first_err)
+                first_err = e;
+        }
+    }
+    return first_err;
+}
+
+/* Gated sliding-window decode for the listed rows (row_ids == NULL: all).
+ * Row r is group r % G of token r / G; its request is r / (G * query_len),
+ * its token within the request j = (r / G) % query_len, its position
+ * p = seq_lens[request] - query_len + j; it attends, per head, over the
+ * tokens [max(0, p - window + 1), p] of its request (none when p < 0), then
+ * the optional headwise gate applies as for the sparse path.  Every row is
+ * active.  out: [n_out][heads][192] float64. */
+int oracle_swa_decode(
+    const uint16_t *query, int64_t q_s0, int64_t q_s1, int rows, int heads,
+    const void *cache, int cache_fp8, int64_t pages, int groups, int block,
+    int64_t c_s0, int64_t c_s1, int64_t c_s2,
+    const int32_t *block_table, int64_t bt_s0, int table_rows, int table_cols,
+    const int32_t *seq_lens, int num_requests,
+    double scale, int query_len, int window, double k_scale, double v_scale,
+    const uint16_t *gate, int64_t g_s0, int64_t g_s1,
+    const int32_t *row_ids, int n_out, double *out)
+{
+    static const int32_t no_region = -1;
+    static const uint8_t one = 1;
+    oracle_problem p = make_problem(query, q_s0, q_s1, rows, heads, cache, cache_fp8, pages,
+                                    groups, block, c_s0, c_s1, c_s2, &no_region, 0, 1,
+                                    block_table, bt_s0, table_rows, table_cols, &no_region, &one,
+                                    scale, query_len, 1, k_scale, v_scale, gate, g_s0, g_s1);
+    int err = check_problem(&p);
+    if (err)
+        return err;
+    if (!seq_lens || window < 1 || num_requests < 0)
+        return ORACLE_ERR_ARGS;
+    if (!row_ids)
+        n_out = rows;
+    int first_err = ORACLE_OK;
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < n_out; ++i) {
+        int row = row_ids ? row_ids[i] : i;
+        double *o = out + (size_t)i * heads * ORACLE_DIM;
+        int e = ORACLE_OK;
+        int64_t req = row / ((int64_t)groups * query_len);
+        if (row < 0 || row >= rows || req >= num_requests) {
+            e = ORACLE_ERR_ARGS;
+        } else {
+            int64_t j = (row / groups) % query_len;
+            int64_t pos = (int64_t)seq_lens[req] - query_len + j + (MUT(19) ? 1 : 0);
+            int64_t lo = pos - window + (MUT(18) ? 0 : 1);
+            if (lo < 0)
+                lo = 0;
+            int64_t n = pos >= lo ? pos - lo + 1 : 0;
+            int64_t *tok = malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+            if (!tok) {
+                e = ORACLE_ERR_ALLOC;
+            } else {
+                for (int64_t k = 0; k < n; ++k)
+                    tok[k] = lo + k;
+                e = attend(&p, row, tok, n, o, NULL);
+                free(tok);
+            }
+            if (!e && gate) {
+                int64_t token = row / groups;
+                int g = row % groups;
+                for (int h = 0; h < heads; ++h) {
+                    double f = oracle_gate_factor(gate[token * g_s0 + (int64_t)(g * heads + h) * g_s1]);
+                    for (int d = 0; d < ORACLE_DIM; ++d)
+                        o[(size_t)h * ORACLE_DIM + d] *= f;
+                }
+            }
+        }
         if (e) {
 #pragma omp critical
             if (!first_err)

@@ -39,8 +39,6 @@ namespace {
 constexpr int kDim = 192;
 constexpr int kRow = 384;
 constexpr int kMaxHeads = 16;
-constexpr int kSlots = 64;                 // token slots per pipeline stage
-constexpr int kBandBytes = kSlots * 128;   // one 128-byte column band of a stage
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxSplits = 64;
@@ -51,32 +49,57 @@ constexpr float kRescaleSlack = 8.0f;      // log2 units a running max may lag t
 constexpr size_t kHeaderBytes = 256;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
+
 template <bool FP8>
 struct Traits;
+// A stage holds kSlots tokens as kBands column bands of 128 bytes per token.
+// Two consumer warps share a stage (kWarpTokens slots each) and the two warp
+// pairs take alternate stages, so a stage is released as soon as its pair is
+// done with it.
 template <>
-struct Traits<true> {                      // 384 B per token: 3 bands, 4 stages of 24 KB
+struct Traits<true> {                      // FP8: 384 B per token; 4 stages of 64 tokens (24 KB)
     static constexpr int kBands = 3;
     static constexpr int kStages = 4;
     static constexpr int kElt = 1;
+    static constexpr int kSlots = 64;
+    static constexpr int kWarpTokens = 32;
+    static constexpr int kBandBytes = kSlots * 128;
 };
 template <>
-struct Traits<false> {                     // 768 B per token: 6 bands, 2 stages of 48 KB
+struct Traits<false> {                     // bf16: 768 B per token; 4 stages of 32 tokens (24 KB)
     static constexpr int kBands = 6;
-    static constexpr int kStages = 2;
+    static constexpr int kStages = 4;
     static constexpr int kElt = 2;
+    static constexpr int kSlots = 32;
+    static constexpr int kWarpTokens = 16;
+    static constexpr int kBandBytes = kSlots * 128;
 };
+constexpr int kWarpsPerStage = 2;
+constexpr int kPairs = kConsumerWarps / kWarpsPerStage;
 
+constexpr int align_up(int x, int a)
+{
+    return (x + a - 1) / a * a;
+}
+
+// Shared memory of the split kernel, from a 1024-byte aligned base: the stage
+// ring (1024-aligned stages for the 128-byte swizzle), mbarriers, stage
+// headers, control words, per-warp softmax statistics, gate factors, the Q
+// fragment array (16-byte vector accesses) and the row's live region list.
 template <bool FP8>
 struct Layout {
-    static constexpr int kStageBytes = Traits<FP8>::kBands * kBandBytes;
+    static constexpr int kStageBytes = Traits<FP8>::kBands * Traits<FP8>::kBandBytes;
     static constexpr int kRing = Traits<FP8>::kStages * kStageBytes;
     static constexpr int kBarOff = kRing;
-    static constexpr int kHdrOff = kBarOff + 16 * Traits<FP8>::kStages;
-    static constexpr int kCtlOff = kHdrOff + 8 * Traits<FP8>::kStages;
+    static constexpr int kHdrOff = align_up(kBarOff + 16 * Traits<FP8>::kStages, 16);
+    static constexpr int kCtlOff = align_up(kHdrOff + 8 * Traits<FP8>::kStages, 16);
     static constexpr int kMlOff = kCtlOff + 64;
-    static constexpr int kGammaOff = kMlOff + kConsumerWarps * kMaxHeads * 2 * 4;
-    static constexpr int kQOff = kGammaOff + kMaxHeads * 4;      // Q fragments [12][32] x 16 B
-    static constexpr int kLiveOff = kQOff + 12 * 32 * 16;
+    static constexpr int kGammaOff = align_up(kMlOff + kConsumerWarps * kMaxHeads * 2 * 4, 16);
+    static constexpr int kQOff = align_up(kGammaOff + kMaxHeads * 4, 128);   // [12][32] x 16 B
+    static constexpr int kLiveOff = align_up(kQOff + 12 * 32 * 16, 16);
+    static_assert(kStageBytes % 1024 == 0 && Traits<FP8>::kBandBytes % 1024 == 0, "swizzle atoms");
+    static_assert(Traits<FP8>::kSlots == kWarpsPerStage * Traits<FP8>::kWarpTokens, "stage split");
+    static_assert(kBarOff % 8 == 0 && kHdrOff % 8 == 0 && kQOff % 16 == 0, "alignment");
     static_assert(kRing >= kConsumerWarps * kMaxHeads * kObufStride * 4, "epilogue buffer");
     static size_t bytes(int num_regions) {
         return 1024 + kLiveOff + 4 * (size_t)((num_regions + 31) & ~31);
@@ -298,6 +321,60 @@ __device__ __forceinline__ int rowmap(int n)
     return (n >> 1) | ((n & 1) << 2);
 }
 
+// O[16 heads x 192] += P[16 x 16 slots] V[16 slots x 192] for one warp.  V is
+// read with ldmatrix.trans from the stage's V bands: lane `mi = lane / 8`
+// addresses k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of a chunk pair;
+// `vrow` is this lane's slot row, `vsw` its swizzle phase.  MASKED zeroes the
+// V values of invalid slots (vm0: k-slots 2t, 2t+1; vm1: 8+2t, 9+2t).
+template <bool FP8, bool MASKED>
+__device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t (&pa)[4], uint32_t vrow,
+                                              int mi, int vsw, uint32_t vm0, uint32_t vm1)
+{
+    if constexpr (FP8) {
+        // 16-dim chunks cv = 0..11: V dims 0..63 sit in band 1 chunks 4..7,
+        // dims 64..191 in band 2 chunks 0..7.  One chunk gives two n8 tiles:
+        // even dims (tile 2*cv) and odd dims (tile 2*cv + 1).
+#pragma unroll
+        for (int c2 = 0; c2 < 6; ++c2) {
+            const int cv = 2 * c2 + (mi >> 1);
+            const int band = cv < 4 ? 1 : 2;
+            const int ch = cv < 4 ? cv + 4 : cv - 4;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(vrow + band * Traits<FP8>::kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+            if constexpr (MASKED) {
+                r0 &= vm0;
+                r1 &= vm1;
+                r2 &= vm0;
+                r3 &= vm1;
+            }
+            const uint32_t x0 = prmt(r0, 0x3120u), x1 = prmt(r1, 0x3120u);
+            const uint32_t x2 = prmt(r2, 0x3120u), x3 = prmt(r3, 0x3120u);
+            mma16816<true>(o[4 * c2 + 0], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
+            mma16816<true>(o[4 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
+            mma16816<true>(o[4 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
+            mma16816<true>(o[4 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
+        }
+    } else {
+        // 8-dim chunks cv = 0..23 in bands 3..5; one n8 tile each.
+#pragma unroll
+        for (int c2 = 0; c2 < 12; ++c2) {
+            const int cv = 2 * c2 + (mi >> 1);
+            const int band = 3 + (cv >> 3);
+            const int ch = cv & 7;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(vrow + band * Traits<FP8>::kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+            if constexpr (MASKED) {
+                r0 &= vm0;
+                r1 &= vm1;
+                r2 &= vm0;
+                r3 &= vm1;
+            }
+            mma16816<false>(o[2 * c2], pa, r0, r1);
+            mma16816<false>(o[2 * c2 + 1], pa, r2, r3);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Split kernel
 // ---------------------------------------------------------------------------
@@ -329,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int s = 0; s < T::kStages; ++s) {
             mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, kConsumerWarps);
+            mbar_init(empty_bar + 8 * s, kWarpsPerStage);
         }
         mbar_init_fence();
     }
@@ -374,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int o = 16; o; o >>= 1)
             pieces += __shfl_xor_sync(~0u, pieces, o);
         if (lane == 0) {
-            ctl[0] = static_cast<int>((pieces * P + kSlots - 1) / kSlots);
+            ctl[0] = static_cast<int>((pieces * P + T::kSlots - 1) / T::kSlots);
             ctl[1] = lo;
             ctl[2] = hi;
         }
@@ -417,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int64_t req = row / (p.groups * p.query_len);
         const int grp = row % p.groups;
         const int32_t *bt = p.block_table + req * p.bt_s0;
-        const int pps = kSlots / P;
+        const int pps = T::kSlots / P;
         const uint32_t piece_bytes = static_cast<uint32_t>(P) * kRow * T::kElt;
         int stage = 0, fill = 0, issued = 0;
         uint32_t phase = 0;
@@ -464,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 const uint32_t dst = sbase + stage * L::kStageBytes + fill * P * 128;
 #pragma unroll
                                 for (int b = 0; b < T::kBands; ++b)
-                                    tma_load_4d(dst + b * kBandBytes, &tmap, b * (128 / T::kElt), of,
+                                    tma_load_4d(dst + b * T::kBandBytes, &tmap, b * (128 / T::kElt), of,
                                                 grp, pg, fb);
                                 const uint64_t bitsv = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
                                 mask |= bitsv << (fill * P);
@@ -512,14 +589,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.0f, 0.0f};
 
+    // This warp's pair takes stages pair, pair + 2, ...; inside a stage it owns
+    // slots [slot0, slot0 + kWarpTokens): NT token tiles of 8 for QK^T and KS
+    // k-steps of 16 for PV.
+    constexpr int NT = T::kWarpTokens / 8;
+    constexpr int KS = T::kWarpTokens / 16;
+    const int pair = warp / kWarpsPerStage;
+    const int slot0 = (warp % kWarpsPerStage) * T::kWarpTokens;
+    constexpr uint64_t kWarpMask = (T::kWarpTokens >= 64) ? ~0ull : ((1ull << T::kWarpTokens) - 1ull);
+
     // Per-lane part of the V ldmatrix addresses: matrix mi = lane / 8 covers
     // k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of the chunk pair.
     const int mi = lane >> 3;
     const int vk = (mi & 1) * 8 + (lane & 7);
-    const int vslot = 16 * warp + (vk & 8) + rowmap(vk & 7);
+    const int vslot = slot0 + (vk & 8) + rowmap(vk & 7);
     const int vsw = vslot & 7;
+    const int sw = rowmap(g);              // swizzle phase of this lane's K rows
 
-    for (int st = 0; st < n_st; ++st) {
+    for (int st = pair; st < n_st; st += kPairs) {
         const int s = st % T::kStages;
         const uint32_t par = static_cast<uint32_t>(st / T::kStages) & 1u;
         const bool ok = mbar_wait(full_bar + 8 * s, par, p.wait_ns);
@@ -528,35 +615,37 @@ __global__ void __launch_bounds__(kThreads, 2)
                 atomicOr(p.flags, SDA_FLAG_TIMEOUT);
             break;
         }
-        const uint32_t wm = static_cast<uint32_t>(hdr[s] >> (16 * warp)) & 0xFFFFu;
+        const uint32_t wm = static_cast<uint32_t>((hdr[s] >> slot0) & kWarpMask);
         const uint32_t stage_base = sbase + s * L::kStageBytes;
         if (wm) {
-            // ---- S = Q K^T for this warp's 16 slots (two n8 tiles).  Thread
-            // (g, t) reads column g's token: tile i uses slot 16w + 8i + rowmap(g).
-            float sc[2][4];
+            // ---- S = Q K^T for this warp's slots: tile i, column g is slot
+            // slot0 + 8i + rowmap(g).
+            float sc[NT][4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < NT; ++i)
                 sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
-            const int sw = rowmap(g);
-            const uint32_t row0 = stage_base + (16 * warp + sw) * 128;
-            const uint32_t row1 = row0 + 8 * 128;
+            const uint32_t row0 = stage_base + (slot0 + sw) * 128;
             if constexpr (FP8) {
-                // thread t: band 0 chunks t and t+4, band 1 chunk t (16 dims each)
+                // thread t: band 0 chunks t and t+4, band 1 chunk t (16 dims each);
+                // tiles in pairs to bound the live K words.
 #pragma unroll
-                for (int c = 0; c < 3; ++c) {
-                    const int band = c == 2 ? 1 : 0;
-                    const int ch = c == 1 ? t + 4 : t;
-                    const uint32_t off = band * kBandBytes + ((ch ^ sw) << 4);
-                    const uint4 k0 = lds128(row0 + off);
-                    const uint4 k1 = lds128(row1 + off);
-                    const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
-                    const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+                for (int i0 = 0; i0 < NT; i0 += 2) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const uint4 qv = lds128(qfrag + ((4 * c + j) * 32 + lane) * 16);
-                        const uint32_t qf[4] = {qv.x, qv.y, qv.z, qv.w};
-                        mma16816<true>(sc[0], qf, e4m3x2_to_f16x2(w0[j]), e4m3x2_to_f16x2(w0[j] >> 16));
-                        mma16816<true>(sc[1], qf, e4m3x2_to_f16x2(w1[j]), e4m3x2_to_f16x2(w1[j] >> 16));
+                    for (int c = 0; c < 3; ++c) {
+                        const int band = c == 2 ? 1 : 0;
+                        const int ch = c == 1 ? t + 4 : t;
+                        const uint32_t off = band * T::kBandBytes + ((ch ^ sw) << 4);
+                        const uint4 ka = lds128(row0 + i0 * 8 * 128 + off);
+                        const uint4 kb = lds128(row0 + (i0 + 1) * 8 * 128 + off);
+                        const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
+                        const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 qv = lds128(qfrag + ((4 * c + j) * 32 + lane) * 16);
+                            const uint32_t qf[4] = {qv.x, qv.y, qv.z, qv.w};
+                            mma16816<true>(sc[i0], qf, e4m3x2_to_f16x2(wa[j]), e4m3x2_to_f16x2(wa[j] >> 16));
+                            mma16816<true>(sc[i0 + 1], qf, e4m3x2_to_f16x2(wb[j]), e4m3x2_to_f16x2(wb[j] >> 16));
+                        }
                     }
                 }
             } else {
@@ -565,24 +654,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 6; ++j) {
                     const int band = j >> 1;
                     const int ch = (j & 1) * 4 + t;
-                    const uint32_t off = band * kBandBytes + ((ch ^ sw) << 4);
-                    const uint4 k0 = lds128(row0 + off);
-                    const uint4 k1 = lds128(row1 + off);
+                    const uint32_t off = band * T::kBandBytes + ((ch ^ sw) << 4);
+                    uint4 kv[NT];
+#pragma unroll
+                    for (int i = 0; i < NT; ++i)
+                        kv[i] = lds128(row0 + i * 8 * 128 + off);
                     const uint4 qa = lds128(qfrag + ((2 * j) * 32 + lane) * 16);
                     const uint4 qb = lds128(qfrag + ((2 * j + 1) * 32 + lane) * 16);
                     const uint32_t qfa[4] = {qa.x, qa.y, qa.z, qa.w};
                     const uint32_t qfb[4] = {qb.x, qb.y, qb.z, qb.w};
-                    mma16816<false>(sc[0], qfa, k0.x, k0.y);
-                    mma16816<false>(sc[1], qfa, k1.x, k1.y);
-                    mma16816<false>(sc[0], qfb, k0.z, k0.w);
-                    mma16816<false>(sc[1], qfb, k1.z, k1.w);
+#pragma unroll
+                    for (int i = 0; i < NT; ++i)
+                        mma16816<false>(sc[i], qfa, kv[i].x, kv[i].y);
+#pragma unroll
+                    for (int i = 0; i < NT; ++i)
+                        mma16816<false>(sc[i], qfb, kv[i].z, kv[i].w);
                 }
             }
 
-            // ---- Mask, online softmax.  c0/c2 are slot 8i+t, c1/c3 slot 8i+t+4.
+            // ---- Mask, online softmax.  In tile i, c0/c2 are slot 8i+t and
+            // c1/c3 slot 8i+t+4 (relative to slot0).
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < NT; ++i) {
                 const bool v0 = (wm >> (8 * i + t)) & 1u;
                 const bool v1 = (wm >> (8 * i + t + 4)) & 1u;
                 sc[i][0] = v0 ? sc[i][0] * sl2 : -INFINITY;
@@ -613,60 +707,42 @@ __global__ void __launch_bounds__(kThreads, 2)
                     o[n][3] *= a1;
                 }
             }
-            float pr[2][4];
+            const float r0 = m_run[0] == -INFINITY ? 0.0f : m_run[0];
+            const float r1 = m_run[1] == -INFINITY ? 0.0f : m_run[1];
+            uint32_t pa[KS][4];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                pr[i][0] = m_run[0] == -INFINITY ? 0.0f : fast_exp2(sc[i][0] - m_run[0]);
-                pr[i][1] = m_run[0] == -INFINITY ? 0.0f : fast_exp2(sc[i][1] - m_run[0]);
-                pr[i][2] = m_run[1] == -INFINITY ? 0.0f : fast_exp2(sc[i][2] - m_run[1]);
-                pr[i][3] = m_run[1] == -INFINITY ? 0.0f : fast_exp2(sc[i][3] - m_run[1]);
-            }
-            l_run[0] += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
-            l_run[1] += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
-            const uint32_t pa[4] = {pack2<FP8>(pr[0][0], pr[0][1]), pack2<FP8>(pr[0][2], pr[0][3]),
-                                    pack2<FP8>(pr[1][0], pr[1][1]), pack2<FP8>(pr[1][2], pr[1][3])};
-
-            // ---- O += P V.  Invalid slots' V may hold anything (even NaN):
-            // zero them when this warp's 16 slots are not all valid.
-            uint32_t vm0 = ~0u, vm1 = ~0u;
-            if (wm != 0xFFFFu) {
-                vm0 = (((wm >> t) & 1u) ? 0x0000FFFFu : 0u) | (((wm >> (t + 4)) & 1u) ? 0xFFFF0000u : 0u);
-                vm1 = (((wm >> (t + 8)) & 1u) ? 0x0000FFFFu : 0u) | (((wm >> (t + 12)) & 1u) ? 0xFFFF0000u : 0u);
-            }
-            const uint32_t vrow = stage_base + vslot * 128;
-            if constexpr (FP8) {
-                // 16-dim chunks cv = 0..11: V dims 0..63 sit in band 1 chunks 4..7,
-                // dims 64..191 in band 2 chunks 0..7.  One chunk gives two n8
-                // tiles: even dims (2*cv) and odd dims (2*cv + 1).
+            for (int k2 = 0; k2 < KS; ++k2) {
+                float pr[2][4];
 #pragma unroll
-                for (int c2 = 0; c2 < 6; ++c2) {
-                    const int cv = 2 * c2 + (mi >> 1);
-                    const int band = cv < 4 ? 1 : 2;
-                    const int ch = cv < 4 ? cv + 4 : cv - 4;
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_trans(vrow + band * kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
-                    r0 &= vm0;
-                    r1 &= vm1;
-                    r2 &= vm0;
-                    r3 &= vm1;
-                    const uint32_t x0 = prmt(r0, 0x3120u), x1 = prmt(r1, 0x3120u);
-                    const uint32_t x2 = prmt(r2, 0x3120u), x3 = prmt(r3, 0x3120u);
-                    mma16816<true>(o[4 * c2 + 0], pa, e4m3x2_to_f16x2(x0), e4m3x2_to_f16x2(x1));
-                    mma16816<true>(o[4 * c2 + 1], pa, e4m3x2_to_f16x2(x0 >> 16), e4m3x2_to_f16x2(x1 >> 16));
-                    mma16816<true>(o[4 * c2 + 2], pa, e4m3x2_to_f16x2(x2), e4m3x2_to_f16x2(x3));
-                    mma16816<true>(o[4 * c2 + 3], pa, e4m3x2_to_f16x2(x2 >> 16), e4m3x2_to_f16x2(x3 >> 16));
+                for (int h = 0; h < 2; ++h) {
+                    const int i = 2 * k2 + h;
+                    pr[h][0] = fast_exp2(sc[i][0] - r0);   // -inf scores give 0
+                    pr[h][1] = fast_exp2(sc[i][1] - r0);
+                    pr[h][2] = fast_exp2(sc[i][2] - r1);
+                    pr[h][3] = fast_exp2(sc[i][3] - r1);
                 }
-            } else {
-                // 8-dim chunks cv = 0..23 in bands 3..5; one n8 tile each.
+                l_run[0] += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+                l_run[1] += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+                pa[k2][0] = pack2<FP8>(pr[0][0], pr[0][1]);
+                pa[k2][1] = pack2<FP8>(pr[0][2], pr[0][3]);
+                pa[k2][2] = pack2<FP8>(pr[1][0], pr[1][1]);
+                pa[k2][3] = pack2<FP8>(pr[1][2], pr[1][3]);
+            }
+
+            // ---- O += P V, one 16-slot k-step at a time.  Invalid slots' V may
+            // hold anything (even NaN): zero them when a k-step is not all valid.
 #pragma unroll
-                for (int c2 = 0; c2 < 12; ++c2) {
-                    const int cv = 2 * c2 + (mi >> 1);
-                    const int band = 3 + (cv >> 3);
-                    const int ch = cv & 7;
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_trans(vrow + band * kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
-                    mma16816<false>(o[2 * c2], pa, r0 & vm0, r1 & vm1);
-                    mma16816<false>(o[2 * c2 + 1], pa, r2 & vm0, r3 & vm1);
+            for (int k2 = 0; k2 < KS; ++k2) {
+                const uint32_t km = (wm >> (16 * k2)) & 0xFFFFu;
+                const uint32_t vrow = stage_base + (vslot + 16 * k2) * 128;
+                if (km == 0xFFFFu) {
+                    pv_accumulate<FP8, false>(o, pa[k2], vrow, mi, vsw, 0u, 0u);
+                } else if (km) {
+                    const uint32_t vm0 = (((km >> t) & 1u) ? 0x0000FFFFu : 0u) |
+                                         (((km >> (t + 4)) & 1u) ? 0xFFFF0000u : 0u);
+                    const uint32_t vm1 = (((km >> (t + 8)) & 1u) ? 0x0000FFFFu : 0u) |
+                                         (((km >> (t + 12)) & 1u) ? 0xFFFF0000u : 0u);
+                    pv_accumulate<FP8, true>(o, pa[k2], vrow, mi, vsw, vm0, vm1);
                 }
             }
         }
@@ -770,56 +846,59 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Combine kernel: one CTA per row merges the splits through their LSEs,
+// Combine kernel: one CTA per row, one thread per (head, 4 dims).  Merges the
+// splits through their LSEs (weights exp(lse_s - max), all -inf -> zeros),
 // applies the gate and clears inactive rows.
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(128) sda_combine_kernel(const __grid_constant__ Params p)
+constexpr int kCombineThreads = kMaxHeads * (kDim / 4);   // 768
+
+__global__ void __launch_bounds__(kCombineThreads) sda_combine_kernel(const __grid_constant__ Params p)
 {
-    __shared__ float wts[kMaxHeads][kMaxSplits];
-    __shared__ float gam[kMaxHeads];
     pdl_wait();   // partials come from the split kernel
     const int row = blockIdx.x;
-    const bool act = p.active[row * p.act_s0] != 0;
-    uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0;
-    const int total = p.heads * kDim;
-    if (!act) {
+    const int item = threadIdx.x;
+    if (item >= p.heads * (kDim / 4))
+        return;
+    const int h = item / (kDim / 4);
+    const int d = 4 * (item - h * (kDim / 4));
+    uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0 + static_cast<int64_t>(h) * p.o_s1 + d;
+    if (p.active[row * p.act_s0] == 0) {
         if (p.clear_inactive)
-            for (int e = threadIdx.x; e < total; e += blockDim.x) {
-                const int h = e / kDim, d = e - h * kDim;
-                out[static_cast<int64_t>(h) * p.o_s1 + d] = 0;
-            }
+            out[0] = out[1] = out[2] = out[3] = 0;
         return;
     }
-    if (threadIdx.x < p.heads) {
-        const int h = threadIdx.x;
-        const float *l = p.lse + static_cast<int64_t>(row) * p.splits * p.heads + h;
-        float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s)
-            M = fmaxf(M, l[s * p.heads]);
-        float sum = 0.0f;
-        for (int s = 0; s < p.splits; ++s) {
-            const float w = M == -INFINITY ? 0.0f : expf(l[s * p.heads] - M);
-            wts[h][s] = w;
-            sum += w;
+    const int S = p.splits;
+    const float *l = p.lse + static_cast<int64_t>(row) * S * p.heads + h;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+        M = fmaxf(M, l[s * p.heads]);
+    const float4 *part = reinterpret_cast<const float4 *>(
+        p.partial + (static_cast<int64_t>(row) * S * p.heads + h) * kDim + d);
+    const int64_t step = static_cast<int64_t>(p.heads) * (kDim / 4);   // float4s between splits
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    float wsum = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+        for (int s = 0; s < S; ++s) {
+            const float w = expf(l[s * p.heads] - M);
+            const float4 v = part[s * step];
+            wsum += w;
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
-        const float inv = sum > 0.0f ? 1.0f / sum : 0.0f;
-        for (int s = 0; s < p.splits; ++s)
-            wts[h][s] *= inv;
-        const int64_t tok = row / p.groups;
-        const int grp = row % p.groups;
-        gam[h] = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
-                        : 1.0f;
     }
-    __syncthreads();
-    const float *part = p.partial + static_cast<int64_t>(row) * p.splits * p.heads * kDim;
-    for (int e = threadIdx.x; e < total; e += blockDim.x) {
-        const int h = e / kDim, d = e - h * kDim;
-        float v = 0.0f;
-        for (int s = 0; s < p.splits; ++s)
-            v += wts[h][s] * part[(static_cast<int64_t>(s) * p.heads + h) * kDim + d];
-        out[static_cast<int64_t>(h) * p.o_s1 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v * gam[h]));
-    }
+    const int64_t tok = row / p.groups;
+    const int grp = row % p.groups;
+    const float gam = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
+                             : 1.0f;
+    const float f = wsum > 0.0f ? gam / wsum : 0.0f;
+    out[0] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x * f));
+    out[1] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.y * f));
+    out[2] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.z * f));
+    out[3] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.w * f));
 }
 
 // ---------------------------------------------------------------------------
@@ -903,7 +982,7 @@ sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, c
     if (prm.splits > 1) {
         cudaLaunchConfig_t c2 = {};
         c2.gridDim = dim3(static_cast<unsigned>(prm.rows));
-        c2.blockDim = dim3(128);
+        c2.blockDim = dim3(static_cast<unsigned>(prm.heads * (kDim / 4)));
         c2.dynamicSmemBytes = 0;
         c2.stream = stream;
         c2.attrs = attr;
@@ -1034,7 +1113,8 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
     const int64_t rt = region_tokens == 0 ? block : region_tokens;
     if (rt < 1 || rt > (1 << 24))
         return SDA_ERR_INVALID;
-    const int64_t piece = std::min<int64_t>(std::min<int64_t>(rt, block), kSlots);
+    const int64_t stage_tokens = fp8 ? Traits<true>::kSlots : Traits<false>::kSlots;
+    const int64_t piece = std::min<int64_t>(std::min<int64_t>(rt, block), stage_tokens);
     if (piece % 8 != 0 || rt % piece != 0 || block % piece != 0)
         return SDA_ERR_UNSUPPORTED;
     if (regions->shape[1] > (1 << 14) || block_table->shape[1] > INT32_MAX)

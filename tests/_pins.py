@@ -386,6 +386,48 @@ def pin_split_partials(lib):
                 assert np.isneginf(lse[r, s]).all()
 
 
+def _swa(d, lib, window, **kw):
+    return oracle.swa_decode(d.query, d.cache, d.table, d.lengths.astype(np.int32), scale=d.scale,
+                             window=window, query_len=d.ql, k_scale=d.k_scale, v_scale=d.v_scale,
+                             cache_fp8=d.fp8, gate=kw.pop("gate", d.gate), lib=lib, **kw)
+
+
+def pin_swa_dense(lib):
+    """Sliding window: torch float64 SDPA over the dense slice [max(0, p-w+1), p]."""
+    for case in (dict(seed=101, reqs=3, query_len=2, G=2, H=4, B=16, RT=16),
+                 dict(seed=102, reqs=2, query_len=3, G=1, H=16, B=8, RT=8, fp8=True)):
+        d = Dense(**case)
+        for window in (1, 5, 17, 40, 10_000):
+            got = _swa(d, lib, window)
+            for r in range(d.rows):
+                q, g = r // (d.G * d.ql), r % d.G
+                pos = int(d.positions[r])
+                lo = max(0, pos - window + 1)
+                kv = d.kv[q][g][lo:pos + 1]
+                Q = d.query[r].to(torch.float64).unsqueeze(0)
+                ref = torch.nn.functional.scaled_dot_product_attention(
+                    Q, kv[:, :192].unsqueeze(0), kv[:, 192:].unsqueeze(0), scale=d.scale)[0].numpy()
+                assert np.abs(got[r] - ref).max() < 1e-12, (case, window, r)
+                if window == 1:
+                    assert np.array_equal(got[r], np.broadcast_to(d.kv[q][g][pos, 192:].numpy(), got[r].shape))
+
+
+def pin_swa_matches_sparse_path(lib):
+    """A window equals the sparse path with one-token regions listing exactly the window's tokens."""
+    d = Dense(111, reqs=3, query_len=2, G=2, H=3, B=16, RT=16, gate=True)
+    window = 23
+    got = _swa(d, lib, window)
+    R = window + 2
+    regions = np.full((d.rows, R), -1, np.int32)
+    for r in range(d.rows):
+        pos = int(d.positions[r])
+        ids = np.arange(max(0, pos - window + 1), pos + 1)
+        regions[r, :len(ids)] = ids[::-1]
+    ref = d.oracle(lib, regions=regions, region_tokens=1)
+    assert np.abs(got - ref).max() < 1e-12
+
+
 ALL_PINS = [pin_e4m3_decode, pin_bf16, pin_gate, pin_splits, pin_dense_bruteforce,
             pin_gate_applied, pin_single_token, pin_zero_query_mean, pin_invariants,
-            pin_inactive, pin_empty_rows, pin_split_partials]
+            pin_inactive, pin_empty_rows, pin_split_partials, pin_swa_dense,
+            pin_swa_matches_sparse_path]

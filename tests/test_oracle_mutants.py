@@ -3,7 +3,8 @@
 Each mutant is the oracle's C source built with -DORACLE_MUTANT=n, which turns
 on exactly one plausible slip (wrong exponent bias, dropped scale, strict
 causal mask, K/V halves swapped, wrong group or request index, unrounded or
-mis-indexed gate, wrong split boundaries, ...).  The pins must reject each.
+mis-indexed gate, wrong split boundaries, sliding-window start or
+position off by one, ...).  The pins must reject each.
 """
 import os
 import tempfile
@@ -13,7 +14,7 @@ import pytest
 import oracle
 from _pins import ALL_PINS
 
-MUTANTS = list(range(1, 18))
+MUTANTS = list(range(1, 20))
 
 
 @pytest.fixture(scope="module")
