@@ -82,8 +82,10 @@ def describe(cfg, w, splits):
     return {
         "workload": (f"{cfg.name}: {cfg.requests} requests x query_len {cfg.query_len} x G={cfg.groups} "
                      f"= {cfg.rows} rows, {cfg.heads} heads x 192, {'FP8 E4M3' if cfg.fp8 else 'bf16'} "
-                     f"cache, block {cfg.block}, R={cfg.num_regions} regions of {cfg.region_tokens} tokens, "
-                     f"context {cfg.ctx}"),
+                     f"cache, block {cfg.block}, "
+                     + (f"sliding window {cfg.window}" if cfg.window else
+                        f"R={cfg.num_regions} regions of {cfg.region_tokens} tokens")
+                     + f", context {cfg.ctx}"),
         "rows": cfg.rows, "heads": cfg.heads, "groups": cfg.groups, "query_len": cfg.query_len,
         "block": cfg.block, "region_tokens": cfg.region_tokens, "num_regions": cfg.num_regions,
         "cache_dtype": "fp8_e4m3" if cfg.fp8 else "bf16", "gate": cfg.gate,
@@ -94,6 +96,9 @@ def describe(cfg, w, splits):
 
 def visible_tokens(w) -> np.ndarray:
     """Per row: how many selected tokens are visible (bench accounting only)."""
+    if w.window:
+        pos = w.positions.cpu().numpy().astype(np.int64)
+        return np.clip(np.minimum(w.window, pos + 1), 0, None)
     reg = w.regions.cpu().numpy().astype(np.int64)
     pos = w.positions.cpu().numpy().astype(np.int64)[:, None]
     RT = w.region_tokens
@@ -101,6 +106,32 @@ def visible_tokens(w) -> np.ndarray:
     live = (reg >= 0) & (first <= pos)
     n = np.where(live, np.minimum(RT, pos - first + 1), 0).sum(1)
     return n * (w.active.cpu().numpy() != 0)
+
+
+def unique_kv_bytes(w) -> int:
+    """K|V bytes of the distinct visible tokens per (request, group): rows of one
+    request and group (query_len > 1) may select the same tokens, which a
+    launch then reads once from HBM and again from L2."""
+    elt = 1 if w.fp8 else 2
+    pos = w.positions.cpu().numpy().astype(np.int64)
+    act = w.active.cpu().numpy() != 0
+    G, ql, RT = w.groups, w.query_len, w.region_tokens
+    reg = None if w.window else w.regions.cpu().numpy().astype(np.int64)
+    total = 0
+    for req in range(w.rows // (G * ql)):
+        for g in range(G):
+            rows = [req * G * ql + j * G + g for j in range(ql)]
+            rows = [r for r in rows if act[r]]
+            if not rows:
+                continue
+            pmax = max(pos[r] for r in rows)
+            if w.window:
+                lo = max(0, min(pos[r] - w.window + 1 for r in rows))
+                total += max(0, pmax - lo + 1)
+            else:
+                ids = {int(i) for r in rows for i in reg[r] if i >= 0 and i * RT <= pos[r]}
+                total += sum(min(RT, pmax - i * RT + 1) for i in ids)
+    return total * 384 * elt
 
 
 def traffic(w, splits):
@@ -201,6 +232,16 @@ def ncu_traffic(cfg_name, alg_bytes):
         return None
 
 
+def run_oracle(w, hp):
+    import oracle
+    if w.window:
+        return oracle.swa_decode(hp.query, hp.cache, hp.block_table, hp.seq_lens, scale=w.scale,
+                                 window=w.window, query_len=w.query_len, k_scale=w.k_scale,
+                                 v_scale=w.v_scale, cache_fp8=w.fp8, gate=hp.gate, row_ids=hp.row_ids)
+    return oracle.sparse_decode_attention(hp.query, hp.cache, hp.regions, hp.block_table, hp.positions,
+                                          hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
+
+
 def cpu_baseline(w, n_rows, seed=0):
     """The float64 oracle on a bounded sample of the workload's rows."""
     import oracle
@@ -208,8 +249,7 @@ def cpu_baseline(w, n_rows, seed=0):
     rows = np.sort(rng.choice(w.rows, size=min(n_rows, w.rows), replace=False))
     hp = inputs.host_subset(w, rows)
     t0 = time.perf_counter()
-    oracle.sparse_decode_attention(hp.query, hp.cache, hp.regions, hp.block_table, hp.positions,
-                                   hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
+    run_oracle(w, hp)
     dt = time.perf_counter() - t0
     return {"value": len(rows) / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{len(rows)} seeded rows of the same workload ({dt:.2f} s, float64 C, OpenMP over rows)"}
@@ -230,8 +270,7 @@ def run_reference(args, world, rank):
         rows = np.sort(rng.choice(w.rows, size=n_rows, replace=False))
         hp = inputs.host_subset(w, rows)
         t0 = time.perf_counter()
-        oracle.sparse_decode_attention(hp.query, hp.cache, hp.regions, hp.block_table, hp.positions,
-                                       hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
+        run_oracle(w, hp)
         if k >= args.warmup:
             samples.append(time.perf_counter() - t0)
     total = sum(samples)
@@ -269,7 +308,8 @@ def main():
     sda.load()
     cfg = workload_config(args)
     w = inputs.make_workload(cfg, dev)
-    splits = args.splits or sda.sparse_decode_splits(w.rows)
+    splits = args.splits or (sda.sparse_decode_swa_splits(w.rows, w.window) if w.window
+                             else sda.sparse_decode_splits(w.rows))
     ws = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8, device=dev)
     ks = vs = None
     if w.fp8:
@@ -281,10 +321,17 @@ def main():
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
     stream = torch.cuda.current_stream(dev)
 
-    def step(q=w.query, reg=w.regions, bt=w.block_table, pos=w.positions, act=w.active, gate=w.gate, o=out):
-        sda.sparse_decode_attention(q, w.cache, reg, bt, pos, act, o, scale=w.scale,
-                                    query_len=w.query_len, splits=splits, k_scale=ks, v_scale=vs,
-                                    gate=gate, region_tokens=w.region_tokens, workspace=ws, stream=stream)
+    def step(q=w.query, reg=w.regions, bt=w.block_table, pos=w.positions, act=w.active, gate=w.gate, o=out,
+             seq=w.seq_lens, s=None):
+        if w.window:
+            sda.sparse_decode_swa_attention(q, w.cache, bt, seq, o, scale=w.scale, window=w.window,
+                                            query_len=w.query_len, splits=splits, k_scale=ks, v_scale=vs,
+                                            gate=gate, workspace=ws, stream=s or stream)
+        else:
+            sda.sparse_decode_attention(q, w.cache, reg, bt, pos, act, o, scale=w.scale,
+                                        query_len=w.query_len, splits=splits, k_scale=ks, v_scale=vs,
+                                        gate=gate, region_tokens=w.region_tokens, workspace=ws,
+                                        stream=s or stream)
 
     steps = args.steps or (2000 if not flush else 400)
     for _ in range(args.warmup):
@@ -337,6 +384,7 @@ def main():
                           else "inputs larger than L2 (selected K|V per step >> 129 MB)"),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "selected_kv_gbs": kv_gbs,
+        "unique_kv_gbs": unique_kv_bytes(w) * steps * world / (timed_ms / 1e3) / 1e9,
         "selected_kv_frac_of_peak": kv_gbs / world / peak,
         "active_rows_per_s": value * float((w.active.cpu().numpy() != 0).mean()),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -357,10 +405,7 @@ def main():
         graph = torch.cuda.CUDAGraph()
 
         def gstep():
-            sda.sparse_decode_attention(w.query, w.cache, w.regions, w.block_table, w.positions,
-                                        w.active, out, scale=w.scale, query_len=w.query_len,
-                                        splits=splits, k_scale=ks, v_scale=vs, gate=w.gate,
-                                        region_tokens=w.region_tokens, workspace=ws, stream=gstream)
+            step(s=gstream)
 
         with torch.cuda.stream(gstream):
             gstep()
@@ -387,8 +432,9 @@ def main():
 
     # ---- end to end through the public API: pinned host inputs -> device, call, output -> host
     if not args.no_e2e:
-        host = {k: v.cpu().pin_memory() for k, v in dict(q=w.query, reg=w.regions, bt=w.block_table,
-                                                          pos=w.positions, act=w.active).items()}
+        per_step = (dict(q=w.query, bt=w.block_table, seq=w.seq_lens) if w.window else
+                    dict(q=w.query, reg=w.regions, bt=w.block_table, pos=w.positions, act=w.active))
+        host = {k: v.cpu().pin_memory() for k, v in per_step.items()}
         if w.gate is not None:
             host["gate"] = w.gate.cpu().pin_memory()
         dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}

@@ -140,6 +140,42 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Split count for the sliding-window decode below (a reading of its own: the
+ * page's `swa_decode_plan` body is not shown).  Starts from
+ * sparse_decode_splits(rows) and halves while a split would cover fewer than
+ * 256 window tokens.
+ */
+int sparse_decode_swa_splits(int rows, int window);
+
+/*
+ * Gated sliding-window decode over the same packed cache: the non-DSA layers'
+ * fused path of the vLLM page "vllm.models.step5.nvidia.sparse_attention"
+ * (`Step5SplitKVFlashAttentionImpl.forward_with_headwise_gate`, which calls
+ * `swa_decode_gated` with window = sliding_window[0] + 1, GQA packing and a
+ * split window, bf16, query_len <= 4 there).
+ *
+ *   query, cache, block_table, output, scale, query_len, splits, k_scale,
+ *   v_scale, gate, workspace, stream: as in sparse_decode_attention
+ *                (rows = tokens * G; FP8 caches are accepted as well).
+ *   seq_lens     [requests] int32: tokens of each request including the ones
+ *                being decoded.  Token j of request q sits at position
+ *                p = seq_lens[q] - query_len + j and attends over the `window`
+ *                tokens [max(0, p - window + 1), p] of its request (none when
+ *                p < 0: zeros).
+ *   window       >= 1 (at most 2^30).
+ * Every row is active.  The window is walked in pieces of min(B, 64) (FP8) or
+ * min(B, 32) (bf16) tokens, which must be a multiple of 8 dividing B.  Splits
+ * take contiguous chunks of the window's pieces.  Errors as for
+ * sparse_decode_attention.
+ */
+sda_status sparse_decode_swa_attention(const sda_tensor *query, const sda_tensor *cache,
+                                       const sda_tensor *block_table, const sda_tensor *seq_lens,
+                                       const sda_tensor *output, float scale, int window, int query_len,
+                                       int splits, const float *k_scale, const float *v_scale,
+                                       const sda_tensor *gate, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/*
  * Reads the device error flags (SDA_FLAG_*) from a workspace into *flags,
  * optionally clearing them.  Synchronises `stream` (it must be the stream the
  * calls ran on).  Returns SDA_ERR_CUDA if a CUDA call failed.

@@ -16,6 +16,8 @@ from ._binding import (  # noqa: F401
     set_wait_limit_ns,
     sparse_decode_attention,
     sparse_decode_splits,
+    sparse_decode_swa_attention,
+    sparse_decode_swa_splits,
     status_string,
     workspace_bytes,
 )

@@ -57,6 +57,12 @@ def _declare(lib):
                                             ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                             ctypes.c_size_t, ctypes.c_void_p]
     lib.sparse_decode_attention.restype = ctypes.c_int
+    lib.sparse_decode_swa_splits.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.sparse_decode_swa_splits.restype = ctypes.c_int
+    lib.sparse_decode_swa_attention.argtypes = [P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, P,
+                                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.sparse_decode_swa_attention.restype = ctypes.c_int
     lib.sparse_decode_read_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                               ctypes.c_int, ctypes.c_void_p]
     lib.sparse_decode_read_errors.restype = ctypes.c_int
@@ -166,6 +172,37 @@ def sparse_decode_attention(query, cache, regions, block_table, positions, activ
                                      int(splits), ks, vs, _ref(gd), int(bool(clear_inactive)),
                                      int(region_tokens), workspace.data_ptr(),
                                      workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+
+
+def sparse_decode_swa_splits(rows: int, window: int) -> int:
+    return load().sparse_decode_swa_splits(int(rows), int(window))
+
+
+def sparse_decode_swa_attention(query, cache, block_table, seq_lens, output, *, scale: float,
+                                window: int, query_len: int = 1, splits: int | None = None,
+                                k_scale=None, v_scale=None, gate=None,
+                                workspace: torch.Tensor | None = None,
+                                stream: torch.cuda.Stream | None = None) -> None:
+    """Gated sliding-window decode into `output` (see include/sdattn.h).
+
+    `splits=None` uses the library's window split policy."""
+    lib = load()
+    rows, heads = query.shape[0], query.shape[1]
+    if splits is None:
+        splits = lib.sparse_decode_swa_splits(rows, int(window))
+    need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
+    if workspace is None:
+        workspace = default_workspace(query.device, need)
+    ks, _keep_k = _scale_ptr(k_scale, query.device)
+    vs, _keep_v = _scale_ptr(v_scale, query.device)
+    descs = [describe(x) for x in (query, cache, block_table, seq_lens, output)]
+    gd = describe(gate)
+    s = stream if stream is not None else torch.cuda.current_stream(query.device)
+    rc = lib.sparse_decode_swa_attention(*[_ref(d) for d in descs], float(scale), int(window), int(query_len),
+                                         int(splits), ks, vs, _ref(gd), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
 

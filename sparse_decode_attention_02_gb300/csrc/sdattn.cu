@@ -126,12 +126,14 @@ struct Params {
     float *partial;
     float *lse;
     unsigned int *flags;
+    const int32_t *seq_lens;   // window mode: per-request lengths (positions derive from them)
     long long pages;
     unsigned long long wait_ns;
     float scale;
     int num_regions, table_cols;
     int rows, heads, groups, block, region_tokens, piece, query_len, splits;
     int clear_inactive;
+    int window;                // > 0: sliding-window mode (no regions; every row active)
 };
 
 // ---------------------------------------------------------------------------
@@ -379,7 +381,7 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
 // Split kernel
 // ---------------------------------------------------------------------------
 
-template <bool FP8>
+template <bool FP8, bool WINDOW>
 __global__ void __launch_bounds__(kThreads, 2)
     sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
 {
@@ -415,18 +417,37 @@ __global__ void __launch_bounds__(kThreads, 2)
     pdl_launch_dependents();
     pdl_wait();   // inputs may be written by the previous kernel on the stream
 
-    const bool act = p.active[row * p.act_s0] != 0;
-    const int pos = p.positions[row * p.pos_s0];
-    const int P = p.piece;
-    const int npr = p.region_tokens / P;   // pieces per region
+    // Sparse mode: the row's selected regions, its position and active flag.
+    // Window mode: every row is active; token j = (row / G) % query_len of a
+    // request sits at seq_lens[request] - query_len + j and sees the window
+    // [max(0, pos - window + 1), pos], walked as pieces (regions of P tokens).
+    constexpr bool windowed = WINDOW;
+    bool act = true;
+    if constexpr (!WINDOW)
+        act = p.active[row * p.act_s0] != 0;
 
     const int g = lane >> 2;               // fragment row group
     const int t = lane & 3;                // thread in quad
 
+    // Producer-only row state.
+    int64_t req = 0, win_lo = 0;
+    int pos = 0, P = 0, npr = 0, win_base = 0;
+    if (warp == kConsumerWarps) {
+        req = row / (p.groups * p.query_len);
+        pos = windowed ? p.seq_lens[req] - p.query_len + (row / p.groups) % p.query_len
+                       : p.positions[row * p.pos_s0];
+        P = p.piece;
+        npr = p.region_tokens / P;             // pieces per region (1 in window mode)
+        win_lo = windowed ? max(0, pos - p.window + 1) : 0;   // first visible token
+        win_base = static_cast<int>(win_lo / P);              // its piece index
+    }
+
     if (warp == kConsumerWarps) {
         // ---- Producer: compact the live regions of this row, in stored order.
         int n_live = 0;
-        if (act) {
+        if (windowed) {
+            n_live = pos >= 0 ? pos / P - win_base + 1 : 0;
+        } else if (act) {
             const int32_t *reg = p.regions + static_cast<int64_t>(row) * p.reg_s0;
             for (int j0 = 0; j0 < p.num_regions; j0 += 32) {
                 const int j = j0 + lane;
@@ -445,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int hi = static_cast<int>(static_cast<int64_t>(split + 1) * n_live / p.splits);
         long long pieces = 0;
         for (int i = lo + lane; i < hi; i += 32) {
-            const int64_t first = static_cast<int64_t>(live[i]) * p.region_tokens;
+            const int64_t first = static_cast<int64_t>(windowed ? win_base + i : live[i]) * p.region_tokens;
             pieces += min(static_cast<int64_t>(npr), (pos - first) / P + 1);
         }
         for (int o = 16; o; o >>= 1)
@@ -491,7 +512,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         // ---- Producer: stream pieces into the stage ring.
         const int lo = ctl[1], hi = ctl[2];
-        const int64_t req = row / (p.groups * p.query_len);
         const int grp = row % p.groups;
         const int32_t *bt = p.block_table + req * p.bt_s0;
         const int pps = T::kSlots / P;
@@ -503,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int base = lo; base < hi && !aborted; base += 32) {
             const int i = base + lane;
             const bool have_r = i < hi;
-            const int id = have_r ? live[i] : 0;
+            const int id = have_r ? (windowed ? win_base + i : live[i]) : 0;
             const int64_t first = static_cast<int64_t>(id) * p.region_tokens;
             const int pc = have_r ? static_cast<int>(min(static_cast<int64_t>(npr), (pos - first) / P + 1)) : 0;
             for (int j = 0; j < npr && !aborted; ++j) {
@@ -520,7 +540,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                         page = -1;
                     }
                 }
+                // valid slots of the piece: [skip, nv) (skip > 0 only for a window's first piece)
                 const int nv = have ? static_cast<int>(min(static_cast<int64_t>(P), pos - t0 + 1)) : 0;
+                const int skip = have ? static_cast<int>(max(static_cast<int64_t>(0), win_lo - t0)) : 0;
                 unsigned bits = __ballot_sync(~0u, have);
                 while (bits) {
                     const int src = __ffs(bits) - 1;
@@ -528,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int pg = __shfl_sync(~0u, page, src);
                     const int of = __shfl_sync(~0u, off, src);
                     const int n = __shfl_sync(~0u, nv, src);
+                    const int sk = __shfl_sync(~0u, skip, src);
                     if (lane == 0 && !aborted) {
                         if (fill == 0 && issued >= T::kStages &&
                             !mbar_wait(empty_bar + 8 * stage, phase ^ 1u, p.wait_ns)) {
@@ -543,7 +566,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                                 for (int b = 0; b < T::kBands; ++b)
                                     tma_load_4d(dst + b * T::kBandBytes, &tmap, b * (128 / T::kElt), of,
                                                 grp, pg, fb);
-                                const uint64_t bitsv = n >= 64 ? ~0ull : ((1ull << n) - 1ull);
+                                const uint64_t bitsv = (n >= 64 ? ~0ull : ((1ull << n) - 1ull)) &
+                                                       ~((1ull << sk) - 1ull);
                                 mask |= bitsv << (fill * P);
                             }
                             if (++fill == pps) {
@@ -863,7 +887,7 @@ __global__ void __launch_bounds__(kCombineThreads) sda_combine_kernel(const __gr
     const int h = item / (kDim / 4);
     const int d = 4 * (item - h * (kDim / 4));
     uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0 + static_cast<int64_t>(h) * p.o_s1 + d;
-    if (p.active[row * p.act_s0] == 0) {
+    if (p.window == 0 && p.active[row * p.act_s0] == 0) {
         if (p.clear_inactive)
             out[0] = out[1] = out[2] = out[3] = 0;
         return;
@@ -939,7 +963,7 @@ bool dims_ok(const sda_tensor *t, int ndim)
 
 // The dynamic shared memory limit each kernel instantiation has been raised to,
 // per device.
-template <bool FP8>
+template <bool FP8, bool WINDOW>
 cudaError_t ensure_smem(size_t bytes)
 {
     static std::mutex mu;
@@ -952,20 +976,20 @@ cudaError_t ensure_smem(size_t bytes)
     size_t &cur = raised[dev & 63];
     if (bytes <= cur)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(sda_split_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sda_split_kernel<FP8, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes));
     if (e == cudaSuccess)
         cur = bytes;
     return e;
 }
 
-template <bool FP8>
+template <bool FP8, bool WINDOW>
 sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, cudaStream_t stream)
 {
     const size_t smem = Layout<FP8>::bytes(num_regions);
     if (smem > 227 * 1024)
         return SDA_ERR_UNSUPPORTED;
-    if (ensure_smem<FP8>(smem) != cudaSuccess)
+    if (ensure_smem<FP8, WINDOW>(smem) != cudaSuccess)
         return SDA_ERR_CUDA;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -977,7 +1001,7 @@ sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, c
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8>, tmap, prm) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8, WINDOW>, tmap, prm) != cudaSuccess)
         return SDA_ERR_CUDA;
     if (prm.splits > 1) {
         cudaLaunchConfig_t c2 = {};
@@ -1057,18 +1081,29 @@ sda_status sparse_decode_read_errors(const void *workspace, uint32_t *flags, int
     return SDA_OK;
 }
 
-sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *cache,
-                                   const sda_tensor *regions, const sda_tensor *block_table,
-                                   const sda_tensor *positions, const sda_tensor *active,
-                                   const sda_tensor *output, float scale, int query_len,
-                                   int splits, const float *k_scale, const float *v_scale,
-                                   const sda_tensor *gate, int clear_inactive, int region_tokens,
-                                   void *workspace, size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+// One call of either entry point after argument unpacking.  Sparse mode uses
+// regions / positions / active; window mode (window > 0) uses seq_lens.
+struct Call {
+    const sda_tensor *query, *cache, *regions, *block_table, *positions, *active, *seq_lens, *output, *gate;
+    float scale;
+    int query_len, splits, clear_inactive, region_tokens, window;
+    const float *k_scale, *v_scale;
+    void *workspace;
+    size_t workspace_bytes;
+    void *stream;
+};
+
+sda_status run_call(const Call &c)
 {
+    const bool windowed = c.window > 0;
+    const sda_tensor *query = c.query, *cache = c.cache, *block_table = c.block_table, *output = c.output;
     // ---- Shape / dtype / stride contract (the page's asserts and the
     // eligibility test of the direct sparse decode path).
-    if (!dims_ok(query, 3) || !dims_ok(cache, 4) || !dims_ok(regions, 2) || !dims_ok(block_table, 2) ||
-        !dims_ok(positions, 1) || !dims_ok(active, 1) || !dims_ok(output, 3))
+    if (!dims_ok(query, 3) || !dims_ok(cache, 4) || !dims_ok(block_table, 2) || !dims_ok(output, 3))
         return SDA_ERR_INVALID;
     const int64_t rows = query->shape[0], heads = query->shape[1];
     if (query->dtype != SDA_DTYPE_BF16 || output->dtype != SDA_DTYPE_BF16)
@@ -1081,45 +1116,63 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
         return SDA_ERR_INVALID;
     if (query->stride[2] != 1 || output->stride[2] != 1 || cache->stride[3] != 1)
         return SDA_ERR_INVALID;
-    if (regions->dtype != SDA_DTYPE_INT32 || regions->shape[0] != rows || regions->stride[1] != 1)
-        return SDA_ERR_INVALID;
     if (block_table->dtype != SDA_DTYPE_INT32 || block_table->stride[1] != 1)
         return SDA_ERR_INVALID;
-    if (positions->dtype != SDA_DTYPE_INT32 || positions->shape[0] != rows)
-        return SDA_ERR_INVALID;
-    if ((active->dtype != SDA_DTYPE_BOOL && active->dtype != SDA_DTYPE_UINT8) || active->shape[0] != rows)
-        return SDA_ERR_INVALID;
+    if (windowed) {
+        if (!dims_ok(c.seq_lens, 1) || c.seq_lens->dtype != SDA_DTYPE_INT32 || c.window > (1 << 30))
+            return SDA_ERR_INVALID;
+    } else {
+        const sda_tensor *regions = c.regions, *positions = c.positions, *active = c.active;
+        if (!dims_ok(regions, 2) || !dims_ok(positions, 1) || !dims_ok(active, 1))
+            return SDA_ERR_INVALID;
+        if (regions->dtype != SDA_DTYPE_INT32 || regions->shape[0] != rows || regions->stride[1] != 1)
+            return SDA_ERR_INVALID;
+        if (positions->dtype != SDA_DTYPE_INT32 || positions->shape[0] != rows)
+            return SDA_ERR_INVALID;
+        if ((active->dtype != SDA_DTYPE_BOOL && active->dtype != SDA_DTYPE_UINT8) || active->shape[0] != rows)
+            return SDA_ERR_INVALID;
+        if (regions->shape[1] > (1 << 14))
+            return SDA_ERR_UNSUPPORTED;
+    }
     const bool fp8 = cache->dtype == SDA_DTYPE_FP8_E4M3 || cache->dtype == SDA_DTYPE_UINT8;
     if (!fp8 && cache->dtype != SDA_DTYPE_BF16)
         return SDA_ERR_INVALID;
-    if (fp8 && (!k_scale || !v_scale))
+    if (fp8 && (!c.k_scale || !c.v_scale))
         return SDA_ERR_INVALID;
-    if (query_len < 1 || splits < 1 || splits > kMaxSplits || !std::isfinite(scale))
+    if (c.query_len < 1 || c.splits < 1 || c.splits > kMaxSplits || !std::isfinite(c.scale))
         return SDA_ERR_INVALID;
     const int64_t pages = cache->shape[0], groups = cache->shape[1], block = cache->shape[2];
     if (groups < 1 || block < 1 || pages < 1 || pages > INT32_MAX)
         return SDA_ERR_INVALID;
     if (rows % groups != 0)
         return SDA_ERR_INVALID;
-    const int64_t per_req = groups * query_len;
-    if (rows > 0 && (rows + per_req - 1) / per_req > block_table->shape[0])
+    const int64_t per_req = groups * c.query_len;
+    const int64_t requests = rows > 0 ? (rows + per_req - 1) / per_req : 0;
+    if (requests > block_table->shape[0] || (windowed && requests > c.seq_lens->shape[0]))
         return SDA_ERR_INVALID;
+    const sda_tensor *gate = c.gate;
     const bool gated = gate && gate->data;
     if (gated) {
         if (!dims_ok(gate, 2) || gate->dtype != SDA_DTYPE_BF16 || gate->shape[0] != rows / groups ||
             gate->shape[1] != groups * heads)
             return SDA_ERR_INVALID;
     }
-    const int64_t rt = region_tokens == 0 ? block : region_tokens;
-    if (rt < 1 || rt > (1 << 24))
-        return SDA_ERR_INVALID;
     const int64_t stage_tokens = fp8 ? Traits<true>::kSlots : Traits<false>::kSlots;
-    const int64_t piece = std::min<int64_t>(std::min<int64_t>(rt, block), stage_tokens);
-    if (piece % 8 != 0 || rt % piece != 0 || block % piece != 0)
-        return SDA_ERR_UNSUPPORTED;
-    if (regions->shape[1] > (1 << 14) || block_table->shape[1] > INT32_MAX)
-        return SDA_ERR_UNSUPPORTED;
-    if (rows > INT32_MAX / kMaxSplits)
+    int64_t rt, piece;
+    if (windowed) {                        // the window is walked in pieces of P tokens
+        piece = std::min<int64_t>(block, stage_tokens);
+        rt = piece;
+        if (piece % 8 != 0 || block % piece != 0)
+            return SDA_ERR_UNSUPPORTED;
+    } else {
+        rt = c.region_tokens == 0 ? block : c.region_tokens;
+        if (rt < 1 || rt > (1 << 24))
+            return SDA_ERR_INVALID;
+        piece = std::min<int64_t>(std::min<int64_t>(rt, block), stage_tokens);
+        if (piece % 8 != 0 || rt % piece != 0 || block % piece != 0)
+            return SDA_ERR_UNSUPPORTED;
+    }
+    if (block_table->shape[1] > INT32_MAX || rows > INT32_MAX / kMaxSplits)
         return SDA_ERR_UNSUPPORTED;
     // TMA: 16-byte aligned base and byte strides.
     const int elt = fp8 ? 1 : 2;
@@ -1128,13 +1181,14 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
         (cache->stride[2] * elt) % 16 != 0 || cache->stride[0] <= 0 || cache->stride[1] <= 0 ||
         cache->stride[2] <= 0)
         return SDA_ERR_UNSUPPORTED;
-    const size_t need = sparse_decode_workspace_bytes(static_cast<int>(rows), static_cast<int>(heads), splits);
-    if (!workspace || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 || workspace_bytes < need)
+    const size_t need = sparse_decode_workspace_bytes(static_cast<int>(rows), static_cast<int>(heads), c.splits);
+    if (!c.workspace || reinterpret_cast<uintptr_t>(c.workspace) % 256 != 0 || c.workspace_bytes < need)
         return SDA_ERR_WORKSPACE;
     if (rows == 0)
         return SDA_OK;
-    if (!query->data || !cache->data || !regions->data || !block_table->data || !positions->data ||
-        !active->data || !output->data)
+    if (!query->data || !cache->data || !block_table->data || !output->data)
+        return SDA_ERR_INVALID;
+    if (windowed ? !c.seq_lens->data : (!c.regions->data || !c.positions->data || !c.active->data))
         return SDA_ERR_INVALID;
 
     // ---- Tensor map over the whole cache: dims (384, B, G, pages), boxes of
@@ -1161,33 +1215,38 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
     prm.query = static_cast<const uint16_t *>(query->data);
     prm.q_s0 = query->stride[0];
     prm.q_s1 = query->stride[1];
-    prm.regions = static_cast<const int32_t *>(regions->data);
-    prm.reg_s0 = regions->stride[0];
+    if (!windowed) {
+        prm.regions = static_cast<const int32_t *>(c.regions->data);
+        prm.reg_s0 = c.regions->stride[0];
+        prm.num_regions = static_cast<int>(c.regions->shape[1]);
+        prm.positions = static_cast<const int32_t *>(c.positions->data);
+        prm.pos_s0 = c.positions->stride[0];
+        prm.active = static_cast<const uint8_t *>(c.active->data);
+        prm.act_s0 = c.active->stride[0];
+    } else {
+        prm.seq_lens = static_cast<const int32_t *>(c.seq_lens->data);
+        prm.window = c.window;
+    }
     prm.block_table = static_cast<const int32_t *>(block_table->data);
     prm.bt_s0 = block_table->stride[0];
-    prm.positions = static_cast<const int32_t *>(positions->data);
-    prm.pos_s0 = positions->stride[0];
-    prm.active = static_cast<const uint8_t *>(active->data);
-    prm.act_s0 = active->stride[0];
     prm.output = static_cast<uint16_t *>(const_cast<void *>(output->data));
     prm.o_s0 = output->stride[0];
     prm.o_s1 = output->stride[1];
     prm.gate = gated ? static_cast<const uint16_t *>(gate->data) : nullptr;
     prm.g_s0 = gated ? gate->stride[0] : 0;
     prm.g_s1 = gated ? gate->stride[1] : 0;
-    prm.k_scale = k_scale;
-    prm.v_scale = v_scale;
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    prm.k_scale = c.k_scale;
+    prm.v_scale = c.v_scale;
+    uint8_t *ws = static_cast<uint8_t *>(c.workspace);
     prm.flags = reinterpret_cast<unsigned int *>(ws);
-    if (splits > 1) {
-        const size_t n = static_cast<size_t>(rows) * splits * heads;
+    if (c.splits > 1) {
+        const size_t n = static_cast<size_t>(rows) * c.splits * heads;
         prm.partial = reinterpret_cast<float *>(ws + kHeaderBytes);
         prm.lse = reinterpret_cast<float *>(ws + kHeaderBytes + n * kDim * sizeof(float));
     }
     prm.pages = pages;
     prm.wait_ns = g_wait_ns.load();
-    prm.scale = scale;
-    prm.num_regions = static_cast<int>(regions->shape[1]);
+    prm.scale = c.scale;
     prm.table_cols = static_cast<int>(block_table->shape[1]);
     prm.rows = static_cast<int>(rows);
     prm.heads = static_cast<int>(heads);
@@ -1195,12 +1254,58 @@ sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *ca
     prm.block = static_cast<int>(block);
     prm.region_tokens = static_cast<int>(rt);
     prm.piece = static_cast<int>(piece);
-    prm.query_len = query_len;
-    prm.splits = splits;
-    prm.clear_inactive = clear_inactive ? 1 : 0;
+    prm.query_len = c.query_len;
+    prm.splits = c.splits;
+    prm.clear_inactive = c.clear_inactive ? 1 : 0;
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    return fp8 ? launch<true>(tmap, prm, prm.num_regions, s) : launch<false>(tmap, prm, prm.num_regions, s);
+    cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+    if (windowed)
+        return fp8 ? launch<true, true>(tmap, prm, 0, s) : launch<false, true>(tmap, prm, 0, s);
+    return fp8 ? launch<true, false>(tmap, prm, prm.num_regions, s)
+               : launch<false, false>(tmap, prm, prm.num_regions, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *cache,
+                                   const sda_tensor *regions, const sda_tensor *block_table,
+                                   const sda_tensor *positions, const sda_tensor *active,
+                                   const sda_tensor *output, float scale, int query_len,
+                                   int splits, const float *k_scale, const float *v_scale,
+                                   const sda_tensor *gate, int clear_inactive, int region_tokens,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!regions || !positions || !active)
+        return SDA_ERR_INVALID;
+    const Call c{query, cache, regions, block_table, positions, active, nullptr, output, gate,
+                 scale, query_len, splits, clear_inactive, region_tokens, 0,
+                 k_scale, v_scale, workspace, workspace_bytes, stream};
+    return run_call(c);
+}
+
+int sparse_decode_swa_splits(int rows, int window)
+{
+    int splits = sparse_decode_splits(rows);
+    while (splits > 1 && window / splits < 256)
+        splits /= 2;
+    return splits;
+}
+
+sda_status sparse_decode_swa_attention(const sda_tensor *query, const sda_tensor *cache,
+                                       const sda_tensor *block_table, const sda_tensor *seq_lens,
+                                       const sda_tensor *output, float scale, int window, int query_len,
+                                       int splits, const float *k_scale, const float *v_scale,
+                                       const sda_tensor *gate, void *workspace, size_t workspace_bytes,
+                                       void *stream)
+{
+    if (!seq_lens || window < 1)
+        return SDA_ERR_INVALID;
+    const Call c{query, cache, nullptr, block_table, nullptr, nullptr, seq_lens, output, gate,
+                 scale, query_len, splits, 1, 0, window,
+                 k_scale, v_scale, workspace, workspace_bytes, stream};
+    return run_call(c);
 }
 
 }  // extern "C"

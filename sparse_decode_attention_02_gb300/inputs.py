@@ -13,6 +13,8 @@ block_table row):
   fp8     128 requests, G=2, 16 heads, FP8 E4M3, R=32, ctx 32K-64K, gate, 5% inactive
   spec    256 requests x 2 query tokens, G=4, bf16, R=64 with 0-16 -1 pads, gate, 8% inactive
   large   512 requests, G=4, FP8 E4M3, R=128 (half recent, half older), ctx 128K-256K
+  swa     256 requests x 2 query tokens, G=4, bf16, sliding window 4096, ctx 16K-64K, gate
+          (the non-DSA layers' fused gated sliding-window decode; no regions)
 
 Integer metadata (positions, regions, block tables, active flags) comes from
 numpy's PCG64 seeded with the workload index, so it is identical on every
@@ -51,6 +53,7 @@ class Config:
     selection: str = "uniform"       # "uniform" | "recent_half"
     splits: int | None = None        # None: the library's sparse_decode_splits(rows)
     seed: int = 0
+    window: int = 0                  # > 0: sliding-window decode workload (no regions)
 
     @property
     def rows(self) -> int:
@@ -75,8 +78,10 @@ CONFIGS = {
     "large": Config("large", requests=512, query_len=1, groups=4, heads=16, block=64,
                     region_tokens=64, num_regions=128, ctx=(128 * 1024, 256 * 1024), fp8=True,
                     selection="recent_half", seed=4),
+    "swa": Config("swa", requests=256, query_len=2, groups=4, heads=16, block=64, region_tokens=64,
+                  num_regions=0, ctx=(16 * 1024, 64 * 1024), gate=True, window=4096, seed=5),
 }
-ORDER = ["tiny", "gqa", "fp8", "spec", "large"]
+ORDER = ["tiny", "gqa", "fp8", "spec", "large", "swa"]
 
 
 @dataclasses.dataclass
@@ -94,6 +99,11 @@ class Workload:
     scale: float
     splits: int | None           # forced split count, or None for the library's policy
     filled_tiles: np.ndarray     # [n, 2] (page, group) tiles holding generated K|V
+    seq_lens: torch.Tensor       # [requests] int32 context lengths (tokens incl. the decoded ones)
+
+    @property
+    def window(self) -> int:
+        return self.config.window
 
     @property
     def rows(self) -> int:
@@ -229,6 +239,27 @@ def referenced_tiles(cfg: Config, regions: np.ndarray, table: np.ndarray, pos_ro
     return np.unique(t, axis=0)
 
 
+def window_columns(pos: int, window: int, block: int) -> range:
+    """Block-table columns holding the tokens [max(0, pos - window + 1), pos]."""
+    if pos < 0:
+        return range(0)
+    lo = max(0, pos - window + 1)
+    return range(lo // block, pos // block + 1)
+
+
+def window_tiles(cfg: Config, table: np.ndarray, pos_rows: np.ndarray) -> np.ndarray:
+    """Distinct (page, group) tiles some row's window touches."""
+    tiles = set()
+    per_req = cfg.groups * cfg.query_len
+    for r in range(cfg.rows):
+        req, g = r // per_req, r % cfg.groups
+        for col in window_columns(int(pos_rows[r]), cfg.window, cfg.block):
+            page = int(table[req, col])
+            if page >= 0:
+                tiles.add((page, g))
+    return np.array(sorted(tiles), dtype=np.int64).reshape(-1, 2)
+
+
 # ----------------------------------------------------------------------------
 # Values (torch, on the target device)
 # ----------------------------------------------------------------------------
@@ -291,7 +322,10 @@ def make_workload(cfg: Config | str, device="cpu", *, splits: int | None = None,
     rng = np.random.default_rng(cfg.seed)
     lengths, pos_rows = _positions(cfg, rng)
     table, pages = _block_table(cfg, rng, lengths)
-    regions = _regions(cfg, rng, pos_rows)
+    if cfg.window:
+        regions = np.zeros((cfg.rows, 0), dtype=np.int32)
+    else:
+        regions = _regions(cfg, rng, pos_rows)
     active = _active(cfg, rng)
 
     dev = torch.device(device)
@@ -312,6 +346,8 @@ def make_workload(cfg: Config | str, device="cpu", *, splits: int | None = None,
     if fill == "all":
         pg, gr = np.meshgrid(np.arange(pages), np.arange(cfg.groups), indexing="ij")
         tiles = np.stack([pg.ravel(), gr.ravel()], axis=1)
+    elif cfg.window:
+        tiles = window_tiles(cfg, table, pos_rows)
     else:
         tiles = referenced_tiles(cfg, regions, table, pos_rows)
     k_scale, v_scale = _fill_tiles(cache, tiles, cfg, cfg.seed + 7919, cfg.fp8)
@@ -326,6 +362,7 @@ def make_workload(cfg: Config | str, device="cpu", *, splits: int | None = None,
         scale=1.0 / math.sqrt(DIM),
         splits=splits or cfg.splits,
         filled_tiles=tiles,
+        seq_lens=torch.as_tensor(lengths.astype(np.int32), device=dev),
     )
 
 
@@ -358,9 +395,12 @@ class HostProblem:
     gate: torch.Tensor | None
     row_ids: np.ndarray
     kwargs: dict
+    seq_lens: torch.Tensor       # [n] per host request (window workloads)
 
 
 def host_subset(w: Workload, rows) -> HostProblem:
+    """Host copies for the oracle of `rows` (regions for the sparse path; the
+    window's blocks plus per-request seq_lens for a window workload)."""
     cfg = w.config
     rows = np.asarray(rows, dtype=np.int64)
     n = len(rows)
@@ -380,19 +420,24 @@ def host_subset(w: Workload, rows) -> HostProblem:
     tiles = {}
     host_table = np.full((n, table.shape[1]), -1, dtype=np.int32)
     for i in range(n):
-        for rid in regions[i]:
-            if rid < 0:
+        if w.window:
+            cols = list(window_columns(int(positions[i]), w.window, B))
+        else:
+            cols = []
+            for rid in regions[i]:
+                if rid < 0:
+                    continue
+                for j in range(per_region):
+                    col = (int(rid) * RT) // B + j
+                    if col < table.shape[1] and col * B < (int(rid) + 1) * RT:
+                        cols.append(col)
+        for col in cols:
+            page = int(table[req[i], col])
+            if page < 0:
                 continue
-            for j in range(per_region):
-                col = (int(rid) * RT) // B + j
-                if col >= table.shape[1] or col * B >= (int(rid) + 1) * RT:
-                    continue
-                page = int(table[req[i], col])
-                if page < 0:
-                    continue
-                key = (page, int(grp[i]))
-                k = tiles.setdefault(key, len(tiles))
-                host_table[i, col] = k
+            key = (page, int(grp[i]))
+            k = tiles.setdefault(key, len(tiles))
+            host_table[i, col] = k
     keys = np.array(list(tiles.keys()), dtype=np.int64).reshape(-1, 2)
     if len(keys):
         dev = w.cache.device
@@ -416,5 +461,6 @@ def host_subset(w: Workload, rows) -> HostProblem:
         gate[torch.as_tensor(new_rows // G)] = w.gate.cpu()[torch.as_tensor(rows // G)]
     kwargs = dict(scale=w.scale, query_len=ql, region_tokens=RT,
                   k_scale=w.k_scale, v_scale=w.v_scale, cache_fp8=w.fp8)
+    seq = w.seq_lens.cpu().numpy()[req].astype(np.int32)
     return HostProblem(query, cache, reg, torch.as_tensor(host_table), pos, act, gate,
-                       new_rows.astype(np.int32), kwargs)
+                       new_rows.astype(np.int32), kwargs, torch.as_tensor(seq))

@@ -42,6 +42,29 @@ def run(w, *, splits=None, out=None, clear_inactive=True, workspace=None, cache=
     return out, sda.read_errors(workspace)
 
 
+def run_swa(w, *, splits=None, out=None, workspace=None):
+    """The window path on a window workload; returns (output, device flags)."""
+    splits = splits or sda.sparse_decode_swa_splits(w.rows, w.window)
+    if out is None:
+        out = torch.full_like(w.query, float("nan"))
+    if workspace is None:
+        workspace = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8,
+                                device=w.query.device)
+    ks, vs = scales(w)
+    sda.sparse_decode_swa_attention(w.query, w.cache, w.block_table, w.seq_lens, out, scale=w.scale,
+                                    window=w.window, query_len=w.query_len, splits=splits, k_scale=ks,
+                                    v_scale=vs, gate=w.gate, workspace=workspace)
+    torch.cuda.synchronize()
+    return out, sda.read_errors(workspace)
+
+
+def oracle_swa_rows(w, rows) -> np.ndarray:
+    hp = inputs.host_subset(w, rows)
+    return oracle.swa_decode(hp.query, hp.cache, hp.block_table, hp.seq_lens, scale=w.scale,
+                             window=w.window, query_len=w.query_len, k_scale=w.k_scale,
+                             v_scale=w.v_scale, cache_fp8=w.fp8, gate=hp.gate, row_ids=hp.row_ids)
+
+
 def oracle_all(w) -> np.ndarray:
     return oracle.sparse_decode_attention(
         w.query.cpu(), w.cache.cpu(), w.regions.cpu(), w.block_table.cpu(), w.positions.cpu(),

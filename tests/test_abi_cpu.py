@@ -153,3 +153,25 @@ def test_product_path_has_no_cpu_fallback():
             B.load()
     finally:
         B._lib, B.LIB_PATH = saved
+
+
+def test_swa_entry_validation(lib):
+    INV, UNS = B.SDA_ERR_INVALID, B.SDA_ERR_UNSUPPORTED
+    f = FakeDev()
+    seq = f.t(4, (4,))
+    r = ctypes.byref
+
+    def call(window=256, seq_desc=seq, splits=1, cache=None, ql=1):
+        ws = lib.sparse_decode_workspace_bytes(f.rows, f.H, splits)
+        return lib.sparse_decode_swa_attention(r(f.q), r(cache or f.cache), r(f.table),
+                                               r(seq_desc) if seq_desc is not None else None, r(f.out),
+                                               0.07, window, ql, splits, None, None, None, 1 << 24, ws, None)
+    assert call(window=0) == INV
+    assert call(seq_desc=None) == INV
+    assert call(seq_desc=f.t(4, (3,))) == INV                 # fewer lengths than requests
+    assert call(seq_desc=f.t(1, (4,))) == INV                 # wrong dtype
+    assert call(window=(1 << 30) + 1) == INV
+    assert call(cache=f.t(1, (64, 2, 12, 384))) == UNS       # piece 12: not a multiple of 8
+    assert sda.sparse_decode_swa_splits(2048, 4096) == 1
+    assert sda.sparse_decode_swa_splits(4, 100) == 1
+    assert sda.sparse_decode_swa_splits(64, 8192) == 4
