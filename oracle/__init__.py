@@ -59,6 +59,8 @@ def _declare(lib):
                                       vp, i64, i32, i32, vp, i32, dbl, i32, i32, dbl, dbl,
                                       vp, i64, i64, vp, i32, vp]
     lib.oracle_swa_decode.restype = i32
+    lib.oracle_select_regions.argtypes = [vp, i64, i32, i32, vp, vp, i32, vp]
+    lib.oracle_select_regions.restype = i32
     lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_decode.restype = dbl
     lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
@@ -257,6 +259,27 @@ def swa_decode(query, cache, block_table, seq_lens, *, scale, window, query_len=
         len(sl), float(scale), int(query_len), int(window),
         float(k_scale if k_scale is not None else 1.0), float(v_scale if v_scale is not None else 1.0),
         *gate_args, ids.ctypes.data if ids is not None else None, n, out.ctypes.data)
+    if rc:
+        raise OracleError(_ERRORS.get(rc, str(rc)))
+    return out
+
+
+def select_regions(scores, current, topk, topk_lengths=None, lib=None) -> np.ndarray:
+    """Region selection: int32 [rows, topk], the current region first, then the
+    topk - 1 best-scoring other candidates among ids [0, topk_lengths[r]) in
+    ascending id order, padded with -1 (ties go to the lower id)."""
+    lib = lib or load()
+    sc = _np(scores, np.float32)
+    if sc.ndim != 2:
+        raise ValueError("scores must be [rows, N]")
+    if sc.shape[1] and _estrides(sc)[1] != 1:
+        sc = np.ascontiguousarray(sc)
+    cur = np.ascontiguousarray(_np(current, np.int32))
+    ln = None if topk_lengths is None else np.ascontiguousarray(_np(topk_lengths, np.int32))
+    rows, n_cols = sc.shape
+    out = np.zeros((rows, topk), dtype=np.int32)
+    rc = lib.oracle_select_regions(sc.ctypes.data, _estrides(sc)[0], rows, n_cols, cur.ctypes.data,
+                                   ln.ctypes.data if ln is not None else None, int(topk), out.ctypes.data)
     if rc:
         raise OracleError(_ERRORS.get(rc, str(rc)))
     return out

@@ -36,7 +36,13 @@
  *     whose first token is visible, in their stored order) into contiguous
  *     chunks [floor(s*n/S), floor((s+1)*n/S));
  *   - sliding window: token j of request q sits at p = seq_lens[q] -
- *     query_len + j and sees the `window` tokens [max(0, p - window + 1), p].
+ *     query_len + j and sees the `window` tokens [max(0, p - window + 1), p];
+ *   - region selection (the adapter page "vllm.models.step5.nvidia.
+ *     flashinfer_sparse", `select_regions(scores, current, topk,
+ *     topk_lengths=..., sort=False)`, body not shown): candidates are the ids
+ *     [0, topk_lengths[r]); the current region is always kept; the other
+ *     topk - 1 slots take the highest scores; NaN ranks lowest; ties and the
+ *     output order are unstated (this oracle breaks ties by lower id).
  *
  * Everything is float64 except the gate, whose fp32 sigmoid and bf16 rounding
  * are a quantisation the page fixes in those precisions.
@@ -552,6 +558,86 @@ int oracle_swa_decode(
             if (!first_err)
                 first_err = e;
         }
+    }
+    return first_err;
+}
+
+/* One row of region selection: writes the selected ids (current first, then
+ * the others in ascending id order) to out[0..topk), padding with -1.  Plain
+ * definition: rank every candidate other than the current one by (score
+ * descending, id ascending) with a full sort and keep the first topk - 1. */
+typedef struct {
+    float score;
+    int32_t id;
+} oracle_cand;
+
+static int cand_cmp(const void *a, const void *b)
+{
+    const oracle_cand *x = a, *y = b;
+    int xn = isnan(x->score), yn = isnan(y->score);
+    if (xn != yn)
+        return xn - yn;                      /* NaN after everything */
+    if (!xn && x->score != y->score)
+        return x->score > y->score ? -1 : 1;  /* higher score first */
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+static int cmp_i32(const void *a, const void *b)
+{
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+int oracle_select_regions(const float *scores, int64_t s_s0, int rows, int n_cols,
+                          const int32_t *current, const int32_t *topk_lengths, int topk,
+                          int32_t *out)
+{
+    if (!scores || !current || !out || rows < 0 || n_cols < 0 || topk < 1)
+        return ORACLE_ERR_ARGS;
+    int first_err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int r = 0; r < rows; ++r) {
+        int32_t *o = out + (int64_t)r * topk;
+        int len = topk_lengths ? topk_lengths[r] : n_cols;
+        if (len > n_cols)
+            len = n_cols;
+        if (len < 0)
+            len = 0;
+        int cur = current[r];
+        int forced = cur >= 0 && cur < len && !MUT(20);
+        oracle_cand *c = malloc(sizeof(oracle_cand) * (size_t)(len > 0 ? len : 1));
+        int32_t *ids = malloc(sizeof(int32_t) * (size_t)(topk > 0 ? topk : 1));
+        if (!c || !ids) {
+            free(c);
+            free(ids);
+#pragma omp critical
+            first_err = ORACLE_ERR_ALLOC;
+            continue;
+        }
+        int n = 0;
+        for (int i = 0; i < len; ++i) {
+            if (forced && i == cur)
+                continue;
+            c[n].score = scores[(int64_t)r * s_s0 + i];
+            c[n].id = i;
+            ++n;
+        }
+        qsort(c, (size_t)n, sizeof *c, cand_cmp);
+        int keep = topk - forced;
+        if (keep > n)
+            keep = n;
+        int k = 0;
+        if (forced)
+            o[k++] = cur;
+        for (int i = 0; i < keep; ++i)
+            ids[i] = c[MUT(21) ? n - 1 - i : i].id;
+        qsort(ids, (size_t)keep, sizeof *ids, cmp_i32);
+        for (int i = 0; i < keep; ++i)
+            o[k++] = ids[i];
+        while (k < topk)
+            o[k++] = -1;
+        free(ids);
+        free(c);
     }
     return first_err;
 }

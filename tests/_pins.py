@@ -427,7 +427,58 @@ def pin_swa_matches_sparse_path(lib):
     assert np.abs(got - ref).max() < 1e-12
 
 
+def _select_numpy(scores, cur, topk, length):
+    """Brute force with numpy's sort: rank (score desc, id asc), NaN last."""
+    forced = 0 <= cur < length
+    ids = np.array([i for i in range(length) if not (forced and i == cur)], dtype=np.int64)
+    sc = scores[ids].astype(np.float64)
+    key = np.where(np.isnan(sc), np.inf, -sc)
+    order = np.lexsort((ids, key))
+    keep = ids[order[:max(0, topk - int(forced))]]
+    return ([cur] if forced else []) + sorted(keep.tolist())
+
+
+def pin_select_regions(lib):
+    """Region selection against numpy brute force, with its invariants."""
+    rng = np.random.default_rng(7)
+    for rows, n, topk in ((40, 300, 16), (20, 64, 80), (10, 5000, 1024)):
+        scores = rng.standard_normal((rows, n)).astype(np.float32)
+        scores[0, :7] = np.nan
+        scores[1, 10:40] = 0.25                     # ties
+        lengths = rng.integers(0, n + 1, size=rows).astype(np.int32)
+        lengths[2] = n
+        current = np.array([rng.integers(-1, max(1, l)) for l in lengths], dtype=np.int32)
+        current[3] = -1                              # no current region
+        got = oracle.select_regions(scores, current, topk, lengths, lib=lib)
+        for r in range(rows):
+            L, cur = int(lengths[r]), int(current[r])
+            row = [int(x) for x in got[r] if x >= 0]
+            assert all(x == -1 for x in got[r][len(row):]), r
+            forced = 0 <= cur < L
+            assert len(row) == min(topk, L), (r, len(row))
+            if forced:
+                assert row[0] == cur
+            others = row[1:] if forced else row
+            assert others == sorted(others) and len(set(others)) == len(others)
+            chosen = set(others)
+            rest = [i for i in range(L) if i not in chosen and not (forced and i == cur)]
+            if chosen and rest:                       # every kept score >= every dropped one
+                kept = scores[r, sorted(chosen)]
+                drop = scores[r, rest]
+                lo = np.min(np.where(np.isnan(kept), -np.inf, kept))
+                hi = np.max(np.where(np.isnan(drop), -np.inf, drop))
+                assert lo >= hi, r
+            if r != 1:                                # unique answer without ties
+                assert row == _select_numpy(scores[r], cur, topk, L), r
+    # closed forms
+    sc = np.array([[5.0, 4.0, 3.0, 2.0, 1.0]], np.float32)
+    assert oracle.select_regions(sc, np.array([4], np.int32), 2, lib=lib).tolist() == [[4, 0]]
+    assert oracle.select_regions(sc, np.array([0], np.int32), 9, lib=lib).tolist() == [[0, 1, 2, 3, 4, -1, -1, -1, -1]]
+    sc = np.array([[-np.inf, np.nan, 1.0]], np.float32)
+    assert oracle.select_regions(sc, np.array([-1], np.int32), 2, lib=lib).tolist() == [[0, 2]]
+
+
 ALL_PINS = [pin_e4m3_decode, pin_bf16, pin_gate, pin_splits, pin_dense_bruteforce,
             pin_gate_applied, pin_single_token, pin_zero_query_mean, pin_invariants,
             pin_inactive, pin_empty_rows, pin_split_partials, pin_swa_dense,
-            pin_swa_matches_sparse_path]
+            pin_swa_matches_sparse_path, pin_select_regions]

@@ -4,7 +4,8 @@ Each mutant is the oracle's C source built with -DORACLE_MUTANT=n, which turns
 on exactly one plausible slip (wrong exponent bias, dropped scale, strict
 causal mask, K/V halves swapped, wrong group or request index, unrounded or
 mis-indexed gate, wrong split boundaries, sliding-window start or
-position off by one, ...).  The pins must reject each.
+position off by one, region selection that drops the current region or
+keeps the lowest scores, ...).  The pins must reject each.
 """
 import os
 import tempfile
@@ -14,7 +15,7 @@ import pytest
 import oracle
 from _pins import ALL_PINS
 
-MUTANTS = list(range(1, 20))
+MUTANTS = list(range(1, 22))
 
 
 @pytest.fixture(scope="module")
