@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", default="large", choices=inputs.ORDER)
+    ap.add_argument("--config", default="large", choices=inputs.ORDER + ["select"])
     ap.add_argument("--splits", type=int, default=None, help="force a split count")
     ap.add_argument("--requests", type=int, default=None, help="shrink the batch (profiling)")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="context range override (profiling)")
@@ -260,6 +260,29 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
+    if args.config == "select":
+        sw = inputs.make_select_workload("cpu")
+        steps, n = args.steps or 3, args.cpu_rows or 256
+        samples = []
+        for k in range(args.warmup + steps):
+            rows = np.sort(np.random.default_rng(1000 + k).choice(sw.rows, size=n, replace=False))
+            sc, cur, ln = sw.scores[rows], sw.current[rows], sw.lengths[rows]
+            t0 = time.perf_counter()
+            oracle.select_regions(sc, cur, sw.topk, ln)
+            if k >= args.warmup:
+                samples.append(time.perf_counter() - t0)
+        value = n * steps / sum(samples)
+        print(json.dumps({
+            "impl": "reference", "metric": "region selection rows/s (top-1024 of 16K-32K region scores "
+            "per row), 1 GPU", "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * sum(samples) / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "select: 2048 rows, topk 1024", "rows": sw.rows, "topk": sw.topk},
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{n} seeded rows per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     cfg = workload_config(args)
     w = inputs.make_workload(cfg, "cpu" if not torch.cuda.is_available() else "cuda:0")
     steps = args.steps or 3
@@ -289,6 +312,64 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_select(args, dev, world, rank):
+    """Region selection alone: 2048 decode rows (the large workload's rows), ids of
+    8-token regions up to each row's position (16K-32K candidates), top-1024."""
+    import sparse_decode_attention_02_gb300 as sda
+    sw = inputs.make_select_workload(dev)
+    out = torch.empty((sw.rows, sw.topk), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    read = int(sw.lengths.sum().item()) * 4 + sw.rows * 12
+    flush = read < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+
+    def step():
+        sda.sparse_decode_select_regions(sw.scores, sw.current, sw.topk, out, topk_lengths=sw.lengths,
+                                         stream=stream)
+    steps = args.steps or 200
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    with ClockSampler(dev.index) as clocks:
+        for k in range(steps):
+            if flush:
+                scratch.zero_()
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in ev]
+    timed_ms = max_over_ranks(sum(per), dev)
+    peak, peak_kind = measured_peak()
+    alg = read + sw.rows * sw.topk * 4
+    achieved = alg / (statistics.mean(per) / 1e3) / 1e9
+    line = {
+        "metric": "region selection rows/s (top-1024 of 16K-32K region scores per row), 1 GPU",
+        "value": sw.rows * steps * world / (timed_ms / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": timed_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "select: 2048 rows, 8-token regions up to positions in 128K-256K, topk 1024",
+                   "rows": sw.rows, "topk": sw.topk, "max_candidates": int(sw.scores.shape[1]),
+                   "l2": "flushed between steps, per-step CUDA events summed" if flush
+                   else "inputs larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "sda_select_kernel", "algorithmic_bytes_per_launch": alg},
+        "gpu_launches": steps, "clocks": clocks.summary(),
+    }
+    if rank == 0 and not args.no_cpu:
+        import oracle
+        n = args.cpu_rows or 256
+        t0 = time.perf_counter()
+        oracle.select_regions(sw.scores[:n].cpu(), sw.current[:n].cpu(), sw.topk, sw.lengths[:n].cpu())
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n / dt, "unit": "rows/s", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": f"first {n} rows ({dt:.2f} s, full sort per row)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -306,6 +387,12 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sda.load()
+    if args.config == "select":
+        run_select(args, dev, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     cfg = workload_config(args)
     w = inputs.make_workload(cfg, dev)
     splits = args.splits or (sda.sparse_decode_swa_splits(w.rows, w.window) if w.window

@@ -45,7 +45,8 @@ typedef enum {
     SDA_DTYPE_FP8_E4M3 = 2,   /* OCP E4M3 "fn" (finite, bias 7)                        */
     SDA_DTYPE_UINT8 = 3,      /* raw bytes; an FP8 cache may be passed as uint8        */
     SDA_DTYPE_INT32 = 4,
-    SDA_DTYPE_BOOL = 5        /* one byte, nonzero = true                              */
+    SDA_DTYPE_BOOL = 5,       /* one byte, nonzero = true                              */
+    SDA_DTYPE_FP32 = 6
 } sda_dtype;
 
 /* A strided view of device memory.  Unused trailing shape/stride entries are
@@ -174,6 +175,30 @@ sda_status sparse_decode_swa_attention(const sda_tensor *query, const sda_tensor
                                        int splits, const float *k_scale, const float *v_scale,
                                        const sda_tensor *gate, void *workspace, size_t workspace_bytes,
                                        void *stream);
+
+/*
+ * Region selection for decode rows: the step before sparse_decode_attention
+ * on the vLLM page "vllm.models.step5.nvidia.flashinfer_sparse"
+ * (`select_and_run_decode_attention` calls `select_regions(scores, current,
+ * topk, topk_lengths=..., sort=False)`; its body is not on the page, so the
+ * rule below is a reading).
+ *
+ *   scores        [rows, N] fp32, stride[1] == 1: a score per region id.
+ *   current       [rows] int32: the region holding the row's own token; it is
+ *                 always kept when 0 <= current < length.
+ *   topk_lengths  [rows] int32 or NULL (every row has N candidates): the row
+ *                 considers region ids [0, min(length, N)).
+ *   topk          regions per row (>= 1).
+ *   regions       [rows, topk] int32, stride[1] == 1 (written): the current
+ *                 region first, then the topk - 1 best-scoring other
+ *                 candidates in ascending id order, then -1 padding.  NaN
+ *                 scores rank lowest; equal scores go to the lower id.
+ * No workspace; returns SDA_ERR_INVALID for shapes, dtypes or strides outside
+ * this contract, SDA_ERR_CUDA if the launch failed.
+ */
+sda_status sparse_decode_select_regions(const sda_tensor *scores, const sda_tensor *current,
+                                        const sda_tensor *topk_lengths, int topk,
+                                        const sda_tensor *regions, void *stream);
 
 /*
  * Reads the device error flags (SDA_FLAG_*) from a workspace into *flags,

@@ -28,6 +28,7 @@ _DTYPES = {
     torch.uint8: 3,
     torch.int32: 4,
     torch.bool: 5,
+    torch.float32: 6,
 }
 
 
@@ -63,6 +64,8 @@ def _declare(lib):
                                                 ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, P,
                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     lib.sparse_decode_swa_attention.restype = ctypes.c_int
+    lib.sparse_decode_select_regions.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_void_p]
+    lib.sparse_decode_select_regions.restype = ctypes.c_int
     lib.sparse_decode_read_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                               ctypes.c_int, ctypes.c_void_p]
     lib.sparse_decode_read_errors.restype = ctypes.c_int
@@ -205,6 +208,22 @@ def sparse_decode_swa_attention(query, cache, block_table, seq_lens, output, *, 
                                          workspace.numel() * workspace.element_size(), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+
+
+def sparse_decode_select_regions(scores, current, topk: int, regions=None, *, topk_lengths=None,
+                                 stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Region selection into `regions` ([rows, topk] int32, allocated if None);
+    see include/sdattn.h for the rule.  Returns `regions`."""
+    lib = load()
+    if regions is None:
+        regions = torch.empty((scores.shape[0], int(topk)), dtype=torch.int32, device=scores.device)
+    s = stream if stream is not None else torch.cuda.current_stream(scores.device)
+    d = [describe(x) for x in (scores, current, topk_lengths, regions)]
+    rc = lib.sparse_decode_select_regions(_ref(d[0]), _ref(d[1]), _ref(d[2]), int(topk), _ref(d[3]),
+                                          s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+    return regions
 
 
 def read_errors(workspace: torch.Tensor, clear: bool = False,

@@ -464,3 +464,35 @@ def host_subset(w: Workload, rows) -> HostProblem:
     seq = w.seq_lens.cpu().numpy()[req].astype(np.int32)
     return HostProblem(query, cache, reg, torch.as_tensor(host_table), pos, act, gate,
                        new_rows.astype(np.int32), kwargs, torch.as_tensor(seq))
+
+
+# ----------------------------------------------------------------------------
+# Region-selection inputs
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class SelectWorkload:
+    scores: torch.Tensor         # [rows, N] fp32 region scores
+    current: torch.Tensor        # [rows] int32 region holding the row's token
+    lengths: torch.Tensor        # [rows] int32 candidate count (regions up to the token)
+    topk: int
+
+    @property
+    def rows(self) -> int:
+        return self.scores.shape[0]
+
+
+def make_select_workload(device="cpu", *, requests=512, groups=4, ctx=(128 * 1024, 256 * 1024),
+                         region_tokens=8, topk=1024, seed=6) -> SelectWorkload:
+    """Decode-row region scores shaped like the large workload's rows: one row per
+    (token, KV group), ids of `region_tokens`-token regions up to the token's
+    position, scores N(0,1)."""
+    rng = np.random.default_rng(seed)
+    lengths = rng.integers(ctx[0], ctx[1] + 1, size=requests)
+    pos = np.repeat(lengths - 1, groups)
+    cur = (pos // region_tokens).astype(np.int32)
+    n_len = (cur + 1).astype(np.int32)
+    dev = torch.device(device)
+    g = _gen(dev, seed)
+    scores = torch.randn((len(pos), int(n_len.max())), generator=g, device=dev)
+    return SelectWorkload(scores, torch.as_tensor(cur, device=dev), torch.as_tensor(n_len, device=dev), topk)

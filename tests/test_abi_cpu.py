@@ -175,3 +175,22 @@ def test_swa_entry_validation(lib):
     assert sda.sparse_decode_swa_splits(2048, 4096) == 1
     assert sda.sparse_decode_swa_splits(4, 100) == 1
     assert sda.sparse_decode_swa_splits(64, 8192) == 4
+
+
+def test_select_entry_validation(lib):
+    INV = B.SDA_ERR_INVALID
+    f = FakeDev()
+    r = ctypes.byref
+    sc, cur, ln, out = f.t(6, (8, 100)), f.t(4, (8,)), f.t(4, (8,)), f.t(4, (8, 16))
+
+    def call(scores=sc, current=cur, lengths=ln, topk=16, regions=out):
+        return lib.sparse_decode_select_regions(r(scores), r(current), r(lengths) if lengths else None,
+                                                topk, r(regions), None)
+    assert call(topk=0) == INV
+    assert call(scores=f.t(1, (8, 100))) == INV                 # scores must be fp32
+    assert call(scores=f.t(6, (8, 100), (200, 2))) == INV       # inner stride
+    assert call(current=f.t(4, (7,))) == INV
+    assert call(regions=f.t(4, (8, 15))) == INV                 # width != topk
+    assert call(lengths=f.t(1, (8,))) == INV
+    z = f.t(6, (0, 100))
+    assert call(scores=z, current=f.t(4, (0,)), lengths=None, regions=f.t(4, (0, 16))) == B.SDA_OK

@@ -1,0 +1,80 @@
+"""Region selection (CUDA kernel vs the oracle), and selection chained into
+sparse decode attention.
+
+Both sides keep the current region, take the best other scores, rank NaN
+lowest and break ties by the lower id, so the selected ids are compared
+exactly (the rule for ties is this library's reading: the page does not state
+one)."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_decode_attention_02_gb300 as sda
+from gpu_util import check, oracle_rows, run
+from sparse_decode_attention_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def select_both(scores, current, topk, lengths):
+    got = sda.sparse_decode_select_regions(scores, current, topk, topk_lengths=lengths)
+    torch.cuda.synchronize()
+    ref = oracle.select_regions(scores.cpu(), current.cpu(), topk,
+                                None if lengths is None else lengths.cpu())
+    return got.cpu().numpy(), ref
+
+
+@pytest.mark.parametrize("rows,n,topk", [(64, 300, 16), (33, 1000, 1000), (17, 5000, 1024),
+                                         (8, 20000, 1), (5, 70000, 4096)])
+@pytest.mark.parametrize("ties", [0.0, 0.3])
+def test_select_matches_oracle(rows, n, topk, ties):
+    g = torch.Generator(device=DEV).manual_seed(rows * 7 + n)
+    scores = torch.randn(rows, n, generator=g, device=DEV)
+    if ties:
+        scores[torch.rand(rows, n, generator=g, device=DEV) < ties] = -0.75
+    scores[0, :13] = float("nan")
+    scores[1, :5] = float("-inf")
+    scores[2, 10:20] = 0.0
+    scores[2, 20:30] = -0.0
+    lengths = torch.randint(0, n + 1, (rows,), generator=g, device=DEV, dtype=torch.int32)
+    lengths[3] = n
+    current = (torch.rand(rows, generator=g, device=DEV) * (lengths.float() + 1)).to(torch.int32) - 1
+    got, ref = select_both(scores, current, topk, lengths)
+    assert np.array_equal(got, ref)
+    got, ref = select_both(scores, current, topk, None)
+    assert np.array_equal(got, ref)
+
+
+def test_select_large_decode_rows():
+    sw = inputs.make_select_workload(DEV)
+    got, ref = select_both(sw.scores, sw.current, sw.topk, sw.lengths)
+    assert np.array_equal(got, ref)
+    assert (got[:, 0] == sw.current.cpu().numpy()).all()
+
+
+def test_select_then_sparse_decode():
+    """Selection feeding the sparse path (8-token regions) equals the oracle chain."""
+    cfg = inputs.scaled("fp8", requests=6, ctx=(3000, 9000), region_tokens=8, num_regions=64, gate=True)
+    w = inputs.make_workload(cfg, DEV, fill="all")
+    cur = (w.positions // 8).to(torch.int32)
+    lengths = cur + 1
+    scores = torch.randn(w.rows, int(lengths.max()), device=DEV)
+    regions = sda.sparse_decode_select_regions(scores, cur, 64, topk_lengths=lengths)
+    ref_regions = oracle.select_regions(scores.cpu(), cur.cpu(), 64, lengths.cpu())
+    assert np.array_equal(regions.cpu().numpy(), ref_regions)
+    w.regions = regions
+    out, flags = run(w, splits=2)
+    assert flags == 0
+    rows = list(range(w.rows))
+    check(w, out, oracle_rows(w, rows), rows)
