@@ -9,13 +9,18 @@
 // (NaN lowest, ties to the lower id), and the output lists the current region
 // first, then the others in ascending id order, padded with -1.
 //
-// One CTA per row.  A 4-pass radix select (8-bit digits) finds the key of the
-// last kept score: each pass streams the row (8 loads in flight per thread;
-// later passes hit L2) into per-warp shared histograms.  An ordered block scan
-// over 8 consecutive ids per thread then writes the kept ids.
+// One CTA per row, scores compared as order-preserving 32-bit keys.
+//   Fast path (rows of up to 64K candidates): a low threshold is estimated
+//   from a 2048-score sample so that about 2 * topk scores pass it; one
+//   streaming pass keeps the passing (key, id) pairs in shared memory; an
+//   exact radix select on that buffer gives the last kept key; bitmaps over
+//   the ids give the lowest-id ties and the ascending output.
+//   Fallback (buffer overflow or underflow, longer rows): an exact 4-pass
+//   radix select that streams the row each pass, then an ordered compaction.
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "sdattn.h"
 
@@ -23,7 +28,12 @@ namespace {
 
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelBatch = 8;                     // loads in flight per thread and pass
+constexpr int kSelBatch = 8;                     // loads in flight per thread (exact passes)
+constexpr int kFilterBatch = 16;                 // loads in flight per thread (filter pass)
+constexpr int kSample = 2048;                    // scores sampled for the filter threshold
+constexpr int kBufCap = 4096;                    // filtered (key, id) pairs held in shared memory
+constexpr int kFastMaxLen = 65536;               // longest row the bitmaps cover
+constexpr int kBitWords = kFastMaxLen / 32;
 
 struct SelectParams {
     const float *scores;
@@ -35,6 +45,23 @@ struct SelectParams {
     int32_t *out;
     int64_t out_s0;
     int rows, n_cols, topk;
+};
+
+struct SelShared {
+    uint32_t whist[kSelWarps][256];              // per-warp histograms
+    uint32_t hist[256];
+    uint32_t cnt[kSelWarps];
+    uint32_t found[2];                           // digit, keys above it
+    uint32_t counter;
+    union {
+        uint32_t sample[kSample];
+        struct {
+            uint32_t kept[kBitWords];
+            uint32_t tie[kBitWords];
+        } bits;
+    } a;
+    uint32_t buf_key[kBufCap];
+    int32_t buf_id[kBufCap];
 };
 
 // Order-preserving key: a larger score gives a larger key; NaN is the
@@ -50,7 +77,7 @@ __device__ __forceinline__ uint32_t score_key(float x)
 }
 
 // Exclusive block-wide prefix sum of `v` in thread order; *total gets the
-// block's sum.  Uses `cnt` (kSelWarps words) and two barriers.
+// block's sum.  Two barriers.
 __device__ __forceinline__ int block_excl_sum(int v, uint32_t *cnt, int *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -76,14 +103,126 @@ __device__ __forceinline__ int block_excl_sum(int v, uint32_t *cnt, int *total)
     return before + incl - v;
 }
 
+__device__ __forceinline__ void zero_whist(SelShared &sh)
+{
+    for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads)
+        (&sh.whist[0][0])[i] = 0;
+}
+
+// Sums the per-warp histograms and finds the digit holding the key of
+// descending rank `remaining`: sh.found = {digit, keys in higher digits}.
+__device__ __forceinline__ void find_digit(SelShared &sh, int remaining)
+{
+    const int tid = threadIdx.x;
+    __syncthreads();
+    for (int b = tid; b < 256; b += kSelThreads) {
+        uint32_t sum = 0;
+#pragma unroll
+        for (int w = 0; w < kSelWarps; ++w)
+            sum += sh.whist[w][b];
+        sh.hist[b] = sum;
+    }
+    __syncthreads();
+    if (tid < 32) {
+        uint32_t c[8], sum = 0;   // lane l: bins 255 - 8l - j, j = 0..7 (descending)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            c[j] = sh.hist[255 - 8 * tid - j];
+            sum += c[j];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t x = __shfl_up_sync(~0u, incl, o);
+            if (tid >= o)
+                incl += x;
+        }
+        const uint32_t excl = incl - sum;
+        if (excl < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl) {
+            uint32_t acc = excl;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
+                    sh.found[0] = 255u - 8u * tid - j;
+                    sh.found[1] = acc;
+                    break;
+                }
+                acc += c[j];
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// Key of descending rank `rank` (1 <= rank <= n) among keys[0, n) in shared
+// memory; *above gets the number of keys strictly greater.  With `digits` < 4
+// only the top 8 * digits bits are resolved and the lower bits are zero: a
+// lower bound of that key.
+__device__ uint32_t select_shared(SelShared &sh, const uint32_t *keys, int n, int rank, int *above,
+                                  int digits = 4)
+{
+    const int warp = threadIdx.x >> 5;
+    uint32_t prefix = 0, mask = 0;
+    int remaining = rank;
+    for (int shift = 24; shift >= 32 - 8 * digits; shift -= 8) {
+        zero_whist(sh);
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += kSelThreads) {
+            const uint32_t key = keys[i];
+            if ((key & mask) == prefix)
+                atomicAdd(&sh.whist[warp][(key >> shift) & 255u], 1u);
+        }
+        find_digit(sh, remaining);
+        remaining -= static_cast<int>(sh.found[1]);
+        prefix |= sh.found[0] << shift;
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    *above = rank - remaining;
+    return prefix;
+}
+
+// The same over the row's candidates in global memory (all ids < len except cur).
+__device__ uint32_t select_global(SelShared &sh, const float *sc, int len, int cur, bool forced, int rank,
+                                  int *above)
+{
+    const int tid = threadIdx.x, warp = tid >> 5;
+    uint32_t prefix = 0, mask = 0;
+    int remaining = rank;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        zero_whist(sh);
+        __syncthreads();
+        for (int base = 0; base < len; base += kSelThreads * kSelBatch) {
+            float v[kSelBatch];
+#pragma unroll
+            for (int e = 0; e < kSelBatch; ++e) {
+                const int i = base + e * kSelThreads + tid;
+                v[e] = i < len ? sc[i] : 0.0f;
+            }
+#pragma unroll
+            for (int e = 0; e < kSelBatch; ++e) {
+                const int i = base + e * kSelThreads + tid;
+                const uint32_t key = score_key(v[e]);
+                if (i < len && !(forced && i == cur) && (key & mask) == prefix)
+                    atomicAdd(&sh.whist[warp][(key >> shift) & 255u], 1u);
+            }
+        }
+        find_digit(sh, remaining);
+        remaining -= static_cast<int>(sh.found[1]);
+        prefix |= sh.found[0] << shift;
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    *above = rank - remaining;
+    return prefix;
+}
+
 __global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_constant__ SelectParams p)
 {
-    __shared__ uint32_t whist[kSelWarps][256];   // per-warp histograms
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t cnt[kSelWarps];
-    __shared__ uint32_t found_digit, found_above;
+    extern __shared__ __align__(16) unsigned char sel_smem[];
+    SelShared &sh = *reinterpret_cast<SelShared *>(sel_smem);
     const int row = blockIdx.x;
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     const float *sc = p.scores + static_cast<int64_t>(row) * p.s_s0;
     int32_t *out = p.out + static_cast<int64_t>(row) * p.out_s0;
     int len = p.lengths ? p.lengths[row * p.len_s0] : p.n_cols;
@@ -92,118 +231,153 @@ __global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_co
     const bool forced = cur >= 0 && cur < len;
     const int k = p.topk - (forced ? 1 : 0);      // others to keep
     const int cand = len - (forced ? 1 : 0);      // others available
-
-    // Keep every key > thr, and the first `take_eq` keys == thr in id order.
-    const bool take_all = k >= cand;
-    uint32_t thr = 0xFFFFFFFFu;
-    int take_eq = 0;
-    if (!take_all && k > 0) {
-        uint32_t prefix = 0, mask = 0;
-        int remaining = k;                         // rank of the last kept key among matches
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < kSelWarps * 256; i += kSelThreads)
-                (&whist[0][0])[i] = 0;
-            __syncthreads();
-            for (int base = 0; base < len; base += kSelThreads * kSelBatch) {
-                float v[kSelBatch];
-#pragma unroll
-                for (int e = 0; e < kSelBatch; ++e) {
-                    const int i = base + e * kSelThreads + tid;
-                    v[e] = i < len ? sc[i] : __int_as_float(0x7FC00000);
-                }
-#pragma unroll
-                for (int e = 0; e < kSelBatch; ++e) {
-                    const int i = base + e * kSelThreads + tid;
-                    const uint32_t key = score_key(v[e]);
-                    if (i < len && !(forced && i == cur) && (key & mask) == prefix)
-                        atomicAdd(&whist[warp][(key >> shift) & 255u], 1u);
-                }
-            }
-            __syncthreads();
-            for (int b = tid; b < 256; b += kSelThreads) {
-                uint32_t sum = 0;
-#pragma unroll
-                for (int w = 0; w < kSelWarps; ++w)
-                    sum += whist[w][b];
-                hist[b] = sum;
-            }
-            __syncthreads();
-            if (tid < 32) {
-                // lane l holds bins 255 - 8l - j, j = 0..7 (descending)
-                uint32_t c[8], sum = 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = hist[255 - 8 * tid - j];
-                    sum += c[j];
-                }
-                uint32_t incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t x = __shfl_up_sync(~0u, incl, o);
-                    if (tid >= o)
-                        incl += x;
-                }
-                const uint32_t excl = incl - sum;
-                if (excl < static_cast<uint32_t>(remaining) && static_cast<uint32_t>(remaining) <= incl) {
-                    uint32_t acc = excl;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (acc + c[j] >= static_cast<uint32_t>(remaining)) {
-                            found_digit = 255u - 8u * tid - j;
-                            found_above = acc;
-                            break;
-                        }
-                        acc += c[j];
-                    }
-                }
-            }
-            __syncthreads();
-            remaining -= static_cast<int>(found_above);
-            prefix |= found_digit << shift;
-            mask |= 255u << shift;
-            __syncthreads();
-        }
-        thr = prefix;
-        take_eq = remaining;
-    }
-
-    // Ordered compaction: the current region first, then the kept ids
-    // ascending.  Thread t handles ids [tile + 8t, tile + 8t + 8).
     const int base = forced ? 1 : 0;
     if (forced && tid == 0)
         out[0] = cur;
-    int written = 0, eq_seen = 0;
-    for (int tile = 0; tile < len; tile += kSelThreads * kSelBatch) {
-        const int i0 = tile + tid * kSelBatch;
-        unsigned gt_bits = 0, eq_bits = 0;
-#pragma unroll
-        for (int e = 0; e < kSelBatch; ++e) {
-            const int i = i0 + e;
-            const bool valid = i < len && !(forced && i == cur);
-            const uint32_t key = valid ? score_key(sc[i]) : 0u;
-            if (valid && (take_all || (k > 0 && key > thr)))
-                gt_bits |= 1u << e;
-            if (valid && !take_all && k > 0 && key == thr)
-                eq_bits |= 1u << e;
+
+    // Keep every key > thr and the first take_eq keys == thr in id order;
+    // take_all keeps every candidate, k <= 0 keeps none.
+    const bool take_all = k >= cand;
+    uint32_t thr = 0xFFFFFFFFu;
+    int take_eq = 0;
+    int written = 0;
+    bool done = take_all || k <= 0;
+
+    if (!done && len <= kFastMaxLen) {
+        // ---- filter threshold from a sample (all candidates when few)
+        uint32_t t_lo = 0u;
+        if (cand > kBufCap) {
+            for (int j = tid; j < kSample; j += kSelThreads)
+                sh.a.sample[j] = score_key(sc[static_cast<int64_t>(j) * len / kSample]);
+            __syncthreads();
+            const int r = min(kSample, static_cast<int>((2ll * k * kSample + cand - 1) / cand) + 32);
+            int unused;
+            t_lo = select_shared(sh, sh.a.sample, kSample, r, &unused, 2);   // 16-bit lower bound
         }
-        int eq_total, take_total;
-        const int eq_before = block_excl_sum(__popc(eq_bits), cnt, &eq_total);
-        unsigned take_bits = gt_bits;              // ties kept in id order up to take_eq
-        int eq_idx = eq_seen + eq_before;
+        // ---- one streaming pass: (key, id) pairs with key >= t_lo
+        if (tid == 0)
+            sh.counter = 0;
+        __syncthreads();
+        for (int b0 = 0; b0 < len; b0 += kSelThreads * kFilterBatch) {
+            float v[kFilterBatch];
 #pragma unroll
-        for (int e = 0; e < kSelBatch; ++e)
-            if ((eq_bits >> e) & 1u) {
-                if (eq_idx < take_eq)
-                    take_bits |= 1u << e;
-                ++eq_idx;
+            for (int e = 0; e < kFilterBatch; ++e) {
+                const int i = b0 + e * kSelThreads + tid;
+                v[e] = i < len ? sc[i] : 0.0f;
             }
-        int pos = base + written + block_excl_sum(__popc(take_bits), cnt, &take_total);
 #pragma unroll
-        for (int e = 0; e < kSelBatch; ++e)
-            if ((take_bits >> e) & 1u)
-                out[pos++] = i0 + e;
-        written += take_total;
-        eq_seen += eq_total;
+            for (int e = 0; e < kFilterBatch; ++e) {
+                const int i = b0 + e * kSelThreads + tid;
+                const uint32_t key = score_key(v[e]);
+                const bool keep = i < len && !(forced && i == cur) && key >= t_lo;
+                const unsigned m = __ballot_sync(~0u, keep);
+                uint32_t at = 0;
+                if (lane == 0 && m)
+                    at = atomicAdd(&sh.counter, static_cast<uint32_t>(__popc(m)));
+                at = __shfl_sync(~0u, at, 0) + __popc(m & ((1u << lane) - 1u));
+                if (keep && at < static_cast<uint32_t>(kBufCap)) {
+                    sh.buf_key[at] = key;
+                    sh.buf_id[at] = i;
+                }
+            }
+        }
+        __syncthreads();
+        const int total = static_cast<int>(sh.counter);
+        if (total <= kBufCap && total >= k) {
+            // ---- exact select inside the buffer
+            int above;
+            thr = select_shared(sh, sh.buf_key, total, k, &above);
+            take_eq = k - above;
+            const int words = (len + 31) / 32;
+            for (int w = tid; w < words; w += kSelThreads) {
+                sh.a.bits.kept[w] = 0;
+                sh.a.bits.tie[w] = 0;
+            }
+            __syncthreads();
+            for (int e = tid; e < total; e += kSelThreads) {
+                const uint32_t key = sh.buf_key[e];
+                const int id = sh.buf_id[e];
+                if (key > thr)
+                    atomicOr(&sh.a.bits.kept[id >> 5], 1u << (id & 31));
+                else if (key == thr)
+                    atomicOr(&sh.a.bits.tie[id >> 5], 1u << (id & 31));
+            }
+            __syncthreads();
+            // thread t owns words [t * W, t * W + W): ties in id order, then the output
+            const int W = (words + kSelThreads - 1) / kSelThreads;
+            const int w0 = tid * W, w1 = min(words, w0 + W);
+            int ties = 0;
+            for (int w = w0; w < w1; ++w)
+                ties += __popc(sh.a.bits.tie[w]);
+            int tie_total;
+            int rank = block_excl_sum(ties, sh.cnt, &tie_total);
+            int kept = 0;
+            for (int w = w0; w < w1; ++w) {
+                uint32_t tb = sh.a.bits.tie[w];
+                while (tb) {
+                    const int bit = __ffs(tb) - 1;
+                    tb &= tb - 1;
+                    if (rank++ < take_eq)
+                        sh.a.bits.kept[w] |= 1u << bit;
+                }
+                kept += __popc(sh.a.bits.kept[w]);
+            }
+            int kept_total;
+            int pos = base + block_excl_sum(kept, sh.cnt, &kept_total);
+            for (int w = w0; w < w1; ++w) {
+                uint32_t kb = sh.a.bits.kept[w];
+                while (kb) {
+                    const int bit = __ffs(kb) - 1;
+                    kb &= kb - 1;
+                    out[pos++] = w * 32 + bit;
+                }
+            }
+            written = kept_total;
+            done = true;
+        }
+    }
+
+    if (!done) {
+        // ---- exact fallback: streaming radix select over the row
+        int above;
+        thr = select_global(sh, sc, len, cur, forced, k, &above);
+        take_eq = k - above;
+    }
+    if (!done || take_all) {
+        // ---- ordered compaction over the row; thread t handles ids [tile + 8t, tile + 8t + 8)
+        int eq_seen = 0;
+        for (int tile = 0; tile < len; tile += kSelThreads * kSelBatch) {
+            const int i0 = tile + tid * kSelBatch;
+            unsigned gt_bits = 0, eq_bits = 0;
+#pragma unroll
+            for (int e = 0; e < kSelBatch; ++e) {
+                const int i = i0 + e;
+                const bool valid = i < len && !(forced && i == cur);
+                const uint32_t key = valid ? score_key(sc[i]) : 0u;
+                if (valid && (take_all || key > thr))
+                    gt_bits |= 1u << e;
+                if (valid && !take_all && key == thr)
+                    eq_bits |= 1u << e;
+            }
+            int eq_total, take_total;
+            const int eq_before = block_excl_sum(__popc(eq_bits), sh.cnt, &eq_total);
+            unsigned take_bits = gt_bits;          // ties kept in id order up to take_eq
+            int eq_idx = eq_seen + eq_before;
+#pragma unroll
+            for (int e = 0; e < kSelBatch; ++e)
+                if ((eq_bits >> e) & 1u) {
+                    if (eq_idx < take_eq)
+                        take_bits |= 1u << e;
+                    ++eq_idx;
+                }
+            int pos = base + written + block_excl_sum(__popc(take_bits), sh.cnt, &take_total);
+#pragma unroll
+            for (int e = 0; e < kSelBatch; ++e)
+                if ((take_bits >> e) & 1u)
+                    out[pos++] = i0 + e;
+            written += take_total;
+            eq_seen += eq_total;
+        }
     }
     for (int i = base + written + tid; i < p.topk; i += kSelThreads)
         out[i] = -1;
@@ -217,6 +391,24 @@ bool is_dims(const sda_tensor *t, int ndim)
         if (t->shape[i] < 0)
             return false;
     return true;
+}
+
+cudaError_t ensure_select_smem()
+{
+    static std::mutex mu;
+    static bool raised[256] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 256 && raised[dev])
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(sda_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(sizeof(SelShared)));
+    if (e == cudaSuccess && dev >= 0 && dev < 256)
+        raised[dev] = true;
+    return e;
 }
 
 }  // namespace
@@ -239,12 +431,14 @@ extern "C" sda_status sparse_decode_select_regions(const sda_tensor *scores, con
     if (has_len && (!is_dims(topk_lengths, 1) || topk_lengths->dtype != SDA_DTYPE_INT32 ||
                     topk_lengths->shape[0] != rows))
         return SDA_ERR_INVALID;
-    if (rows > INT32_MAX || n_cols > INT32_MAX - kSelThreads * kSelBatch)
+    if (rows > INT32_MAX || n_cols > INT32_MAX - kSelThreads * kFilterBatch)
         return SDA_ERR_UNSUPPORTED;
     if (rows == 0)
         return SDA_OK;
     if (!scores->data || !current->data || !regions->data)
         return SDA_ERR_INVALID;
+    if (ensure_select_smem() != cudaSuccess)
+        return SDA_ERR_CUDA;
     SelectParams prm;
     prm.scores = static_cast<const float *>(scores->data);
     prm.s_s0 = scores->stride[0];
@@ -260,6 +454,7 @@ extern "C" sda_status sparse_decode_select_regions(const sda_tensor *scores, con
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(rows));
     cfg.blockDim = dim3(kSelThreads);
+    cfg.dynamicSmemBytes = sizeof(SelShared);
     cfg.stream = static_cast<cudaStream_t>(stream);
     return cudaLaunchKernelEx(&cfg, sda_select_kernel, prm) == cudaSuccess ? SDA_OK : SDA_ERR_CUDA;
 }
