@@ -406,6 +406,9 @@ cudaError_t ensure_select_smem()
         return cudaSuccess;
     e = cudaFuncSetAttribute(sda_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(SelShared)));
+    if (e == cudaSuccess)   // all of the unified L1/shared storage as shared: 3 CTAs per SM fit
+        e = cudaFuncSetAttribute(sda_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev >= 0 && dev < 256)
         raised[dev] = true;
     return e;

@@ -405,15 +405,17 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int row = blockIdx.x / p.splits;
     const int split = blockIdx.x - row * p.splits;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < T::kStages; ++s) {
-            mbar_init(full_bar + 8 * s, 1);
-            mbar_init(empty_bar + 8 * s, kWarpsPerStage);
+    if (warp == kConsumerWarps) {          // the producer warp owns the pipeline barriers
+        if (lane == 0) {
+            for (int s = 0; s < T::kStages; ++s) {
+                mbar_init(full_bar + 8 * s, 1);
+                mbar_init(empty_bar + 8 * s, kWarpsPerStage);
+            }
+            mbar_init_fence();
+            prefetch_tmap(&tmap);
         }
-        mbar_init_fence();
+        __syncwarp();
     }
-    if (warp == kConsumerWarps && lane == 0)
-        prefetch_tmap(&tmap);
     pdl_launch_dependents();
     pdl_wait();   // inputs may be written by the previous kernel on the stream
 
@@ -447,14 +449,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         int n_live = 0;
         if (windowed) {
             n_live = pos >= 0 ? pos / P - win_base + 1 : 0;
-        } else if (act) {
+        } else {
+            // read whatever `active` says (the loads overlap), then drop inactive rows
             const int32_t *reg = p.regions + static_cast<int64_t>(row) * p.reg_s0;
             for (int j0 = 0; j0 < p.num_regions; j0 += 32) {
                 const int j = j0 + lane;
                 const int id = j < p.num_regions ? reg[j] : -1;
-                if (id < -1)
+                if (act && id < -1)
                     atomicOr(p.flags, SDA_FLAG_BOUNDS);
-                const bool ok = id >= 0 && static_cast<int64_t>(id) * p.region_tokens <= pos;
+                const bool ok = act && id >= 0 && static_cast<int64_t>(id) * p.region_tokens <= pos;
                 const unsigned m = __ballot_sync(~0u, ok);
                 if (ok)
                     live[n_live + __popc(m & ((1u << lane) - 1u))] = id;
@@ -476,6 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             ctl[1] = lo;
             ctl[2] = hi;
         }
+        __syncwarp();
+        // Release the consumers (barriers, stage count) without waiting for
+        // their Q fragments: the producer starts streaming right away.
+        asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
     } else {
         // ---- Consumers: Q A-fragments into shared memory, in fragment order
         // ([k-step][lane] x 4 words).  K-step kk of thread t covers the four
@@ -494,10 +501,11 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int r = 0; r < 2; ++r) {
                 const int m = r ? m1 : m0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    a[r][e] = (act && m < p.heads)
-                                  ? bf16_bits_to_float(q0[static_cast<int64_t>(m) * p.q_s1 + d0 + e])
-                                  : 0.0f;
+                for (int e = 0; e < 4; ++e) {
+                    const float v = m < p.heads ? bf16_bits_to_float(q0[static_cast<int64_t>(m) * p.q_s1 + d0 + e])
+                                                : 0.0f;
+                    a[r][e] = act ? v : 0.0f;
+                }
             }
             const uint32_t addr = qfrag + (kk * 32 + lane) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
@@ -506,8 +514,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                          : "memory");
         }
     }
-    __syncthreads();
-    const int n_st = ctl[0];
+    int n_st = 0;
+    if (warp != kConsumerWarps) {           // wait for the producer's arrive and each other's Q stores
+        asm volatile("bar.sync 2, %0;" ::"n"(kThreads) : "memory");
+        n_st = ctl[0];
+    }
 
     if (warp == kConsumerWarps) {
         // ---- Producer: stream pieces into the stage ring.
