@@ -18,7 +18,8 @@
  *     never synchronises the stream (except sparse_decode_read_errors) and
  *     returns a status instead of aborting.  A launch is asynchronous: results
  *     are valid once the stream has reached that point.
- *   - Inputs are read only; only `output` and `workspace` are written.
+ *   - Inputs are read only; only `output` and `workspace` are written, and
+ *     neither may overlap an input.
  */
 #ifndef SDATTN_H
 #define SDATTN_H

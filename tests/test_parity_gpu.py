@@ -123,6 +123,23 @@ def test_variants(changes, fp8):
         check(w, out, ref, rows)
 
 
+@pytest.mark.parametrize("changes", [
+    dict(groups=8, heads=2),                                        # many KV groups, few heads
+    dict(block=128, region_tokens=128, num_regions=12),             # a region = 2 FP8 / 4 bf16 pieces
+    dict(block=32, region_tokens=64, num_regions=20, query_len=2),  # a region spans two blocks
+    dict(block=64, region_tokens=16, num_regions=150, heads=12),    # four regions per page
+])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_more_layouts(changes, fp8):
+    w = mini("gqa", requests=4, ctx=(2000, 6000), fp8=fp8, gate=True, inactive_frac=0.1, **changes)
+    rows = list(range(w.rows))
+    ref = oracle_rows(w, rows)
+    for s in (1, 3):
+        out, flags = run(w, splits=s)
+        assert flags == 0
+        check(w, out, ref, rows)
+
+
 def test_many_regions_per_row():
     w = mini("gqa", requests=3, ctx=(9000, 12000), region_tokens=8, num_regions=1024, fp8=True)
     rows = list(range(w.rows))
