@@ -8,8 +8,10 @@ the GPU path receives: bf16 as raw 16-bit patterns, FP8 E4M3 as raw bytes.
 
 The definition it computes is the one of the vLLM API page
 "vllm.models.step5.nvidia.ops.sparse_decode_attention" (functions
-``sparse_decode_attention``, ``_gate`` and ``sparse_decode_splits``); the C
-file's header lists the readings taken where that page is silent.
+``sparse_decode_attention``, ``_gate`` and ``sparse_decode_splits``), plus the
+steps around it on the neighbouring pages (sliding-window decode, region
+selection, indexer decode scores); the C file's header lists the readings
+taken where the pages are silent.
 """
 from __future__ import annotations
 
@@ -61,6 +63,9 @@ def _declare(lib):
     lib.oracle_swa_decode.restype = i32
     lib.oracle_select_regions.argtypes = [vp, i64, i32, i32, vp, vp, i32, vp]
     lib.oracle_select_regions.restype = i32
+    lib.oracle_summary_scores.argtypes = [vp, i64, i64, i32, i32, vp, i64, i64, vp, i64, i64,
+                                          vp, i64, i32, i32, vp, i32, i32, i32, vp, i32, vp, vp, vp]
+    lib.oracle_summary_scores.restype = i32
     lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_decode.restype = dbl
     lib.oracle_bf16_decode.argtypes = [ctypes.c_uint16]
@@ -283,6 +288,44 @@ def select_regions(scores, current, topk, topk_lengths=None, lib=None) -> np.nda
     if rc:
         raise OracleError(_ERRORS.get(rc, str(rc)))
     return out
+
+
+def summary_scores(query, weights, summaries, block_table, seq_lens, *, block, n_cols,
+                   query_len=1, row_ids=None, lib=None):
+    """Indexer decode scores: (scores float64 [n, n_cols], current int32 [n],
+    lengths int32 [n]) for the rows (token, g) in ``row_ids`` (all rows when None).
+
+    query [tokens, G, 8, 256] E4M3 bytes (heads and dims contiguous), weights
+    [tokens, G, 8] fp32, summaries [slots, G, 256] E4M3 bytes (one slot per
+    8-token region of every page, slot = page * (block / 8) + offset / 8)."""
+    lib = lib or load()
+    q = _np(query, np.uint8)
+    w = _np(weights, np.float32)
+    m = _np(summaries, np.uint8)
+    bt = _np(block_table, np.int32)
+    sl = np.ascontiguousarray(_np(seq_lens, np.int32))
+    if q.ndim != 4 or q.shape[2:] != (8, 256) or _estrides(q)[2:] != [256, 1]:
+        raise ValueError("query must be [tokens, G, 8, 256] with heads and dims contiguous")
+    tokens, groups = q.shape[:2]
+    if w.shape != (tokens, groups, 8) or _estrides(w)[2] != 1:
+        raise ValueError("weights must be [tokens, G, 8] with unit head stride")
+    if m.ndim != 3 or m.shape[1:] != (groups, 256) or _estrides(m)[1:] != [256, 1]:
+        raise ValueError("summaries must be [slots, G, 256] with groups and dims contiguous")
+    if bt.shape[1] and _estrides(bt)[1] != 1:
+        bt = np.ascontiguousarray(bt)
+    ids, n = _rows_arg(row_ids, tokens * groups)
+    out = np.zeros((n, n_cols), dtype=np.float64)
+    cur = np.zeros(n, dtype=np.int32)
+    lens = np.zeros(n, dtype=np.int32)
+    qs, ws, ms = _estrides(q), _estrides(w), _estrides(m)
+    rc = lib.oracle_summary_scores(
+        q.ctypes.data, qs[0], qs[1], tokens, groups, w.ctypes.data, ws[0], ws[1], m.ctypes.data,
+        ms[0], m.shape[0], bt.ctypes.data, _estrides(bt)[0], bt.shape[0], bt.shape[1], sl.ctypes.data,
+        int(block), int(query_len), int(n_cols), ids.ctypes.data if ids is not None else None, n,
+        out.ctypes.data, cur.ctypes.data, lens.ctypes.data)
+    if rc:
+        raise OracleError(_ERRORS.get(rc, str(rc)))
+    return out, cur, lens
 
 
 def e4m3_decode(code: int, lib=None) -> float:

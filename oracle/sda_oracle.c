@@ -42,7 +42,19 @@
  *     topk_lengths=..., sort=False)`, body not shown): candidates are the ids
  *     [0, topk_lengths[r]); the current region is always kept; the other
  *     topk - 1 slots take the highest scores; NaN ranks lowest; ties and the
- *     output order are unstated (this oracle breaks ties by lower id).
+ *     output order are unstated (this oracle breaks ties by lower id);
+ *   - indexer decode scores (the adapter page, `decode_logits` /
+ *     `decode_summary_scores`, body not shown; the pages give the shapes and
+ *     dtypes and name an FP8 paged MQA-logits kernel): the score of region j
+ *     for row (token, g) is sum_h w[h] * max(0, <q_h, m_j>) over the 8 index
+ *     heads, with q_h the token's FP8 E4M3 index query of group g, w its fp32
+ *     head weights and m_j the FP8 E4M3 mean summary of group g of the
+ *     8-token region j; region j's summary sits in summary slot
+ *     page * (block / 8) + (8j mod block) / 8 with page = block_table[req,
+ *     8j / block]; regions [0, pos / 8] are scored (pos as for the sliding
+ *     window), the rest of the row is -inf.  This formula is a reading, not
+ *     printed on the pages: the CPU tests pin the oracle to it, nothing pins
+ *     it to the pages' own kernel.
  *
  * Everything is float64 except the gate, whose fp32 sigmoid and bf16 rounding
  * are a quantisation the page fixes in those precisions.
@@ -50,6 +62,8 @@
  * Parity status: every function here is pinned by the CPU tests in
  * tests/test_oracle_pins.py (textbook dense attention, closed forms,
  * invariants, torch's e4m3/bf16 decoders, the page's split truth table).
+ * oracle_summary_scores is pinned to its reading only (parity with the pages'
+ * indexer kernel unpinned: its formula is not on the pages).
  */
 #include <math.h>
 #include <stdint.h>
@@ -638,6 +652,97 @@ int oracle_select_regions(const float *scores, int64_t s_s0, int rows, int n_col
             o[k++] = -1;
         free(ids);
         free(c);
+    }
+    return first_err;
+}
+
+/* Indexer decode scores for the rows (token, g) listed in row_ids (all
+ * tokens * groups rows when row_ids is NULL), written densely to
+ * scores[n_out, n_cols] with the -inf tail, plus the row's current region and
+ * scored length.  Plain definition: for every scored region, resolve its
+ * summary slot through the block table, decode the 256 summary bytes and each
+ * head's 256 query bytes, take the dot product, clamp at zero, weight, sum over
+ * the 8 heads. */
+#define ORACLE_IDX_HEADS 8
+#define ORACLE_IDX_DIM 256
+#define ORACLE_IDX_REGION 8
+
+int oracle_summary_scores(const uint8_t *query, int64_t q_s0, int64_t q_s1, int tokens, int groups,
+                          const float *weights, int64_t w_s0, int64_t w_s1,
+                          const uint8_t *summaries, int64_t m_s0, int64_t n_slots,
+                          const int32_t *block_table, int64_t bt_s0, int n_reqs, int width,
+                          const int32_t *seq_lens, int block, int query_len, int n_cols,
+                          const int32_t *row_ids, int n_out, double *scores, int32_t *current,
+                          int32_t *lengths)
+{
+    if (!query || !weights || !summaries || !block_table || !seq_lens || !scores || tokens < 0 ||
+        groups < 1 || block < ORACLE_IDX_REGION || block % ORACLE_IDX_REGION || query_len < 1 ||
+        n_cols < 0 || n_out < 0 || tokens % query_len || tokens / query_len > n_reqs)
+        return ORACLE_ERR_ARGS;
+    const int per_page = block / ORACLE_IDX_REGION;
+    int first_err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < n_out; ++i) {
+        int64_t row = row_ids ? row_ids[i] : i;
+        double *out = scores + (int64_t)i * n_cols;
+        int err = ORACLE_OK;
+        if (row < 0 || row >= (int64_t)tokens * groups) {
+            err = ORACLE_ERR_ARGS;
+        } else {
+            int tok = (int)(row / groups), g = (int)(row % groups);
+            if (MUT(25))
+                g = 0;
+            int req = tok / query_len;
+            int64_t pos = (int64_t)seq_lens[req] - query_len + tok % query_len + (MUT(26) ? 1 : 0);
+            int64_t n = pos >= 0 ? pos / ORACLE_IDX_REGION + (MUT(24) ? 0 : 1) : 0;
+            if (n > n_cols)
+                n = n_cols;
+            if (current)
+                current[i] = pos >= 0 ? (int32_t)(pos / ORACLE_IDX_REGION) : -1;
+            if (lengths)
+                lengths[i] = (int32_t)n;
+            double q[ORACLE_IDX_HEADS][ORACLE_IDX_DIM], w[ORACLE_IDX_HEADS];
+            for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+                const uint8_t *qh = query + (int64_t)tok * q_s0 + (int64_t)g * q_s1 +
+                                    (int64_t)h * ORACLE_IDX_DIM;
+                for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+                    q[h][d] = oracle_e4m3_decode(qh[d]);
+                w[h] = weights[(int64_t)tok * w_s0 + (int64_t)g * w_s1 +
+                               (MUT(23) ? (h + 1) % ORACLE_IDX_HEADS : h)];
+            }
+            for (int64_t j = 0; j < n_cols; ++j)
+                out[j] = -INFINITY;
+            for (int64_t j = 0; j < n && !err; ++j) {
+                int64_t t0 = j * ORACLE_IDX_REGION;
+                if (t0 / block >= width) {
+                    err = ORACLE_ERR_TABLE;
+                    break;
+                }
+                int64_t page = block_table[(int64_t)req * bt_s0 + t0 / block];
+                int64_t slot = page * per_page + (t0 % block) / ORACLE_IDX_REGION;
+                if (page < 0 || slot >= n_slots) {
+                    err = ORACLE_ERR_PAGE;
+                    break;
+                }
+                const uint8_t *m = summaries + slot * m_s0 + (int64_t)g * ORACLE_IDX_DIM;
+                double md[ORACLE_IDX_DIM];
+                for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+                    md[d] = oracle_e4m3_decode(m[d]);
+                double sum = 0.0;
+                for (int h = 0; h < ORACLE_IDX_HEADS; ++h) {
+                    double dot = 0.0;
+                    for (int d = 0; d < ORACLE_IDX_DIM; ++d)
+                        dot += q[h][d] * md[d];
+                    sum += w[h] * (MUT(22) ? dot : (dot > 0.0 ? dot : 0.0));
+                }
+                out[j] = sum;
+            }
+        }
+        if (err) {
+#pragma omp critical
+            if (!first_err)
+                first_err = err;
+        }
     }
     return first_err;
 }

@@ -9,7 +9,9 @@ disagrees with an independent fact:
     that this file scatters into pages itself (never through the oracle);
   * closed forms (one visible token returns V exactly; a zero query averages V);
   * invariants (region order, -1 placement, row permutation, split merging);
-  * the split-count truth table derived by hand from the page's loop.
+  * the split-count truth table derived by hand from the page's loop;
+  * for the indexer scores, dense torch matrix products over summaries this
+    file scatters into pages, one-hot closed forms and linearity in the weights.
 """
 from __future__ import annotations
 
@@ -478,7 +480,122 @@ def pin_select_regions(lib):
     assert oracle.select_regions(sc, np.array([-1], np.int32), 2, lib=lib).tolist() == [[0, 2]]
 
 
+# ---------------------------------------------------------------------------
+# Indexer decode scores
+# ---------------------------------------------------------------------------
+
+def _finite_e4m3(rng, shape):
+    b = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    b[(b & 0x7F) == 0x7F] = 0                        # no NaN codes
+    return b
+
+
+def _e4m3_f64(b):
+    return torch.from_numpy(np.ascontiguousarray(b)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+class DenseSummaries:
+    """Per-(request, group) dense region summaries, scattered by this file into
+    the pages of a shuffled pool (decoy pages hold NaN codes), with FP8 index
+    queries and fp32 head weights for every (token, group)."""
+
+    def __init__(self, seed, *, seq_lens, G=2, B=16, query_len=1, n_cols=None, decoys=3):
+        rng = np.random.default_rng(seed)
+        self.G, self.B, self.query_len = G, B, query_len
+        self.seq_lens = np.asarray(seq_lens, np.int32)
+        reqs = len(seq_lens)
+        W = max(1, -(-int(max(seq_lens)) // B))
+        per = B // 8
+        self.n_cols = W * per if n_cols is None else n_cols
+        self.dense = _finite_e4m3(rng, (reqs, G, W * per, 256))
+        pages = reqs * W + decoys
+        order = rng.permutation(pages)
+        self.table = order[:reqs * W].reshape(reqs, W).astype(np.int32)
+        self.summaries = np.full((pages * per, G, 256), 0x7F, np.uint8)
+        for r in range(reqs):
+            for c in range(W):
+                p = self.table[r, c]
+                self.summaries[p * per:(p + 1) * per] = self.dense[r, :, c * per:(c + 1) * per].transpose(1, 0, 2)
+        tokens = reqs * query_len
+        self.query = _finite_e4m3(rng, (tokens, G, 8, 256))
+        self.weights = rng.standard_normal((tokens, G, 8)).astype(np.float32)
+
+    def run(self, lib, **kw):
+        return oracle.summary_scores(self.query, self.weights, self.summaries, self.table, self.seq_lens,
+                                     block=self.B, n_cols=self.n_cols, query_len=self.query_len,
+                                     lib=lib, **kw)
+
+    def expected(self, row):
+        """Dense torch float64: relu(M q^T) w over the row's scored regions, -inf after."""
+        tok, g = divmod(row, self.G)
+        req = tok // self.query_len
+        pos = int(self.seq_lens[req]) - self.query_len + tok % self.query_len
+        n = min(pos // 8 + 1, self.n_cols) if pos >= 0 else 0
+        out = torch.full((self.n_cols,), -math.inf, dtype=torch.float64)
+        if n:
+            m = _e4m3_f64(self.dense[req, g, :n])
+            q = _e4m3_f64(self.query[tok, g])
+            w = torch.from_numpy(self.weights[tok, g]).to(torch.float64)
+            out[:n] = torch.relu(m @ q.T) @ w
+        return out.numpy(), (pos // 8 if pos >= 0 else -1), n
+
+
+def pin_summary_dense(lib):
+    """Indexer scores against a dense torch computation over summaries this file
+    scattered into shuffled pages (decoys full of NaN codes)."""
+    cases = (dict(seq_lens=[37, 130, 9], G=2, B=16),
+             dict(seq_lens=[200, 64, 1], G=4, B=64, query_len=2),
+             dict(seq_lens=[95, 260], G=1, B=32, query_len=3, n_cols=20))
+    for i, kw in enumerate(cases):
+        d = DenseSummaries(100 + i, **kw)
+        scores, cur, lens = d.run(lib)
+        for row in range(len(d.query) * d.G):
+            exp, ecur, en = d.expected(row)
+            assert cur[row] == ecur and lens[row] == en, (i, row, cur[row], ecur, lens[row], en)
+            fin = np.isfinite(exp)
+            assert np.array_equal(np.isfinite(scores[row]), fin), (i, row)
+            assert np.allclose(scores[row][fin], exp[fin], rtol=1e-12, atol=1e-9), (i, row)
+        sub = [3, 0, 5]
+        s2, c2, l2 = d.run(lib, row_ids=sub)
+        assert np.array_equal(s2, scores[sub]) and np.array_equal(l2, lens[sub])
+
+
+def pin_summary_closed_forms(lib):
+    """One-hot queries read single summary values back: with q_h = +/-e_d on one
+    head, the score is w_h * max(0, +/-m_j[d]); weights enter linearly."""
+    d = DenseSummaries(7, seq_lens=[41, 17], G=2, B=16)
+    one = 0x38                                        # E4M3 code of 1.0
+    for sign, code in ((1.0, one), (-1.0, one | 0x80)):
+        for g in range(2):
+            q = np.zeros_like(d.query)
+            q[:, g, 5, 77] = code
+            d2 = DenseSummaries(7, seq_lens=[41, 17], G=2, B=16)
+            d2.query = q
+            d2.weights[:, :, 5] = 2.5
+            scores, _, lens = d2.run(lib)
+            for tok in range(2):
+                row = tok * 2 + g
+                n = int(lens[row])
+                m = _e4m3_f64(d.dense[tok, g, :n, 77]).numpy()
+                assert np.array_equal(scores[row, :n], 2.5 * np.maximum(0.0, sign * m)), (sign, g, tok)
+                other = tok * 2 + (1 - g)                    # the other group's query is zero
+                assert np.all(scores[other, :int(lens[other])] == 0.0)
+    rng = np.random.default_rng(3)                    # multiples of 1/8: sums are exact in fp32
+    w1 = (rng.integers(-16, 17, d.weights.shape) / 8).astype(np.float32)
+    w2 = (rng.integers(-16, 17, d.weights.shape) / 8).astype(np.float32)
+    d.weights = w1
+    a, _, _ = d.run(lib)
+    d.weights = w2
+    b, _, _ = d.run(lib)
+    d.weights = w1 + w2
+    c, _, _ = d.run(lib)
+    fin = np.isfinite(a)
+    assert np.allclose(c[fin], (a + b)[fin], rtol=1e-12, atol=1e-6)
+    assert np.all(c[~fin] == -np.inf)
+
+
 ALL_PINS = [pin_e4m3_decode, pin_bf16, pin_gate, pin_splits, pin_dense_bruteforce,
             pin_gate_applied, pin_single_token, pin_zero_query_mean, pin_invariants,
             pin_inactive, pin_empty_rows, pin_split_partials, pin_swa_dense,
-            pin_swa_matches_sparse_path, pin_select_regions]
+            pin_swa_matches_sparse_path, pin_select_regions, pin_summary_dense,
+            pin_summary_closed_forms]

@@ -5,7 +5,9 @@ on exactly one plausible slip (wrong exponent bias, dropped scale, strict
 causal mask, K/V halves swapped, wrong group or request index, unrounded or
 mis-indexed gate, wrong split boundaries, sliding-window start or
 position off by one, region selection that drops the current region or
-keeps the lowest scores, ...).  The pins must reject each.
+keeps the lowest scores, indexer scores without the ReLU, with
+rotated head weights, without the current region, from the wrong group or
+with the token position off by one, ...).  The pins must reject each.
 """
 import os
 import tempfile
@@ -15,7 +17,7 @@ import pytest
 import oracle
 from _pins import ALL_PINS
 
-MUTANTS = list(range(1, 22))
+MUTANTS = list(range(1, 27))
 
 
 @pytest.fixture(scope="module")

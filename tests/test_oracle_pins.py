@@ -29,3 +29,17 @@ def test_oracle_rejects_bad_indices():
     reg[0, 0] = pos[0] // d.RT
     with pytest.raises(oracle.OracleError):
         d.oracle(regions=reg, positions=pos)
+
+
+def test_summary_scores_rejects_bad_indices():
+    import numpy as np
+    from _pins import DenseSummaries
+    d = DenseSummaries(5, seq_lens=[40, 20], G=2, B=16)
+    d.table[0, 1] = d.summaries.shape[0]              # a page past the summary buffer
+    with pytest.raises(oracle.OracleError):
+        d.run(oracle.load())
+    d = DenseSummaries(5, seq_lens=[40, 20], G=2, B=16)
+    d.seq_lens = np.array([40 + 3 * 16, 20], np.int32)  # scored regions past the table width
+    d.n_cols = 20
+    with pytest.raises(oracle.OracleError):
+        d.run(oracle.load())
