@@ -202,6 +202,56 @@ sda_status sparse_decode_select_regions(const sda_tensor *scores, const sda_tens
                                         const sda_tensor *regions, void *stream);
 
 /*
+ * Indexer decode scores: a score per 8-token region for every (token, KV
+ * group) row, the input of sparse_decode_select_regions.  The adapter page
+ * "vllm.models.step5.nvidia.flashinfer_sparse" computes this in
+ * `decode_logits` (fast path `decode_summary_scores`, for FP8 queries of 8
+ * heads x 256 and uint8 summaries [*, G, 256]) through an FP8 paged
+ * MQA-logits kernel whose formula is not on the page; the reading taken is
+ *     score[row, j] = sum_h weights[token, g, h] * max(0, <q_h, m_j>)
+ * over the 8 index heads h, with q_h = query[token, g, h, :] and m_j the
+ * summary of region j of group g, both decoded from E4M3 (no scale), the
+ * product accumulated in fp32.
+ *
+ *   query        [tokens, G, 8, 256] FP8 E4M3 (or uint8 holding E4M3 bytes);
+ *                stride[3] == 1, stride[2] == 256, stride[0] and stride[1]
+ *                multiples of 16, base 16-byte aligned.  Row r = t * G + g.
+ *   weights      [tokens, G, 8] fp32, stride[2] == 1.
+ *   summaries    [slots, G, 256] FP8 E4M3 / uint8, stride[2] == 1,
+ *                stride[1] == 256, stride[0] a multiple of 16, base 16-byte
+ *                aligned.  Slot page * (block_size / 8) + k holds the summary
+ *                of tokens [8k, 8k + 8) of that page.
+ *   block_table  [reqs, W] int32, stride[1] == 1: the request's pages.
+ *   seq_lens     [>= reqs] int32: request lengths; the query_len tokens of
+ *                request q are tokens q * query_len + i at position
+ *                seq_lens[q] - query_len + i.
+ *   block_size   tokens per page, a multiple of 8.
+ *   query_len    tokens per request, 1..4; tokens must be a multiple of it.
+ *   scores       [tokens * G, N] fp32, stride[1] == 1 (written): columns
+ *                j < min(pos / 8 + 1, N) hold the score of region j, the
+ *                rest -inf (all -inf when pos < 0).  Region j's page is
+ *                block_table[req, 8j / block_size].
+ *   current      [tokens * G] int32 or NULL (written): pos / 8, -1 if pos < 0.
+ *   lengths      [tokens * G] int32 or NULL (written): the number of scored
+ *                columns, min(pos / 8 + 1, N) (0 if pos < 0).
+ *   workspace    NULL, or >= 256 bytes, 256-byte aligned: receives
+ *                SDA_FLAG_BOUNDS when a scored region's table column is past
+ *                W or its page has no slots in `summaries` (that region
+ *                scores -inf); read it with sparse_decode_read_errors.
+ * Every summary is read from HBM once per (request, group): the query_len
+ * tokens share it.  Returns SDA_ERR_INVALID for shapes, dtypes or strides
+ * outside this contract, SDA_ERR_UNSUPPORTED for query_len > 4 or
+ * misaligned operands, SDA_ERR_WORKSPACE for a bad workspace, SDA_ERR_CUDA if
+ * the launch failed; tokens == 0 returns SDA_OK with no launch.
+ */
+sda_status sparse_decode_summary_scores(const sda_tensor *query, const sda_tensor *weights,
+                                        const sda_tensor *summaries, const sda_tensor *block_table,
+                                        const sda_tensor *seq_lens, int block_size, int query_len,
+                                        const sda_tensor *scores, const sda_tensor *current,
+                                        const sda_tensor *lengths, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
+/*
  * Reads the device error flags (SDA_FLAG_*) from a workspace into *flags,
  * optionally clearing them.  Synchronises `stream` (it must be the stream the
  * calls ran on).  Returns SDA_ERR_CUDA if a CUDA call failed.

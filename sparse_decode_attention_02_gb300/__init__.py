@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     sparse_decode_attention,
     sparse_decode_select_regions,
     sparse_decode_splits,
+    sparse_decode_summary_scores,
     sparse_decode_swa_attention,
     sparse_decode_swa_splits,
     status_string,

@@ -66,6 +66,9 @@ def _declare(lib):
     lib.sparse_decode_swa_attention.restype = ctypes.c_int
     lib.sparse_decode_select_regions.argtypes = [P, P, P, ctypes.c_int, P, ctypes.c_void_p]
     lib.sparse_decode_select_regions.restype = ctypes.c_int
+    lib.sparse_decode_summary_scores.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, P, P, P,
+                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    lib.sparse_decode_summary_scores.restype = ctypes.c_int
     lib.sparse_decode_read_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                               ctypes.c_int, ctypes.c_void_p]
     lib.sparse_decode_read_errors.restype = ctypes.c_int
@@ -224,6 +227,32 @@ def sparse_decode_select_regions(scores, current, topk: int, regions=None, *, to
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
     return regions
+
+
+def sparse_decode_summary_scores(query, weights, summaries, block_table, seq_lens, *, block_size: int,
+                                 n_cols: int | None = None, query_len: int = 1, scores=None,
+                                 current=None, lengths=None, workspace=None,
+                                 stream: torch.cuda.Stream | None = None):
+    """Indexer decode scores into `scores` ([tokens * G, n_cols] fp32, allocated
+    if None; n_cols defaults to block_table's width * block_size / 8), with the
+    optional `current` / `lengths` outputs; see include/sdattn.h.  Returns
+    `scores`."""
+    lib = load()
+    rows = query.shape[0] * query.shape[1]
+    if scores is None:
+        if n_cols is None:
+            n_cols = block_table.shape[1] * int(block_size) // 8
+        scores = torch.empty((rows, int(n_cols)), dtype=torch.float32, device=query.device)
+    s = stream if stream is not None else torch.cuda.current_stream(query.device)
+    d = [describe(x) for x in (query, weights, summaries, block_table, seq_lens, scores, current, lengths)]
+    ws = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.sparse_decode_summary_scores(_ref(d[0]), _ref(d[1]), _ref(d[2]), _ref(d[3]), _ref(d[4]),
+                                          int(block_size), int(query_len), _ref(d[5]), _ref(d[6]),
+                                          _ref(d[7]), ws, wsb, s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+    return scores
 
 
 def read_errors(workspace: torch.Tensor, clear: bool = False,

@@ -7,7 +7,7 @@ import sys
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
-SOURCES = [os.path.join(HERE, "csrc", "sdattn.cu"), os.path.join(HERE, "csrc", "sda_select.cu")]
+SOURCES = [os.path.join(HERE, "csrc", name) for name in ("sdattn.cu", "sda_select.cu", "sda_index.cu")]
 HEADER = os.path.join(ROOT, "include", "sdattn.h")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsdattn.so")

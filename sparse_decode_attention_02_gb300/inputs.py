@@ -496,3 +496,100 @@ def make_select_workload(device="cpu", *, requests=512, groups=4, ctx=(128 * 102
     g = _gen(dev, seed)
     scores = torch.randn((len(pos), int(n_len.max())), generator=g, device=dev)
     return SelectWorkload(scores, torch.as_tensor(cur, device=dev), torch.as_tensor(n_len, device=dev), topk)
+
+
+# ----------------------------------------------------------------------------
+# Indexer-score inputs
+# ----------------------------------------------------------------------------
+
+INDEX_HEADS = 8
+INDEX_DIM = 256
+
+
+@dataclasses.dataclass
+class IndexWorkload:
+    query: torch.Tensor          # [tokens, G, 8, 256] float8_e4m3fn index queries
+    weights: torch.Tensor        # [tokens, G, 8] fp32 head weights
+    summaries: torch.Tensor      # [pages * block / 8, G, 256] float8_e4m3fn region summaries
+    block_table: torch.Tensor    # [requests, W] int32, -1 past the request's pages
+    seq_lens: torch.Tensor       # [requests] int32
+    block: int
+    query_len: int
+    n_cols: int                  # score columns per row
+
+    @property
+    def tokens(self) -> int:
+        return self.query.shape[0]
+
+    @property
+    def groups(self) -> int:
+        return self.query.shape[1]
+
+    @property
+    def rows(self) -> int:
+        return self.tokens * self.groups
+
+
+def _e4m3_normal(shape, gen, device, std=1.0) -> torch.Tensor:
+    x = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * std
+    return x.clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+
+
+def make_index_workload(device="cpu", *, requests=512, groups=4, query_len=1,
+                        ctx=(128 * 1024, 256 * 1024), block=64, n_cols=None, spare_pages=64,
+                        seed=7, chunk_slots=1 << 20) -> IndexWorkload:
+    """Indexer inputs for decode rows: request lengths U[ctx], each request's
+    pages drawn from one shuffled pool (plus `spare_pages` unused ones), E4M3
+    index queries and summaries from N(0,1), head weights N(0,1)/16.  The
+    default matches the large workload's rows: 512 requests x 4 KV groups,
+    contexts 128K-256K, 64-token pages, 8-token regions (32K score columns)."""
+    rng = np.random.default_rng(seed)
+    lengths = rng.integers(ctx[0], ctx[1] + 1, size=requests).astype(np.int64)
+    n_pages = -(-lengths // block)
+    width = int(n_pages.max()) if requests else 1
+    pool = int(n_pages.sum()) + spare_pages
+    order = rng.permutation(pool).astype(np.int32)
+    table = np.full((requests, width), -1, dtype=np.int32)
+    at = 0
+    for r in range(requests):
+        k = int(n_pages[r])
+        table[r, :k] = order[at:at + k]
+        at += k
+    if n_cols is None:
+        n_cols = width * block // 8
+    dev = torch.device(device)
+    gen = _gen(dev, seed)
+    tokens = requests * query_len
+    query = _e4m3_normal((tokens, groups, INDEX_HEADS, INDEX_DIM), gen, dev)
+    weights = torch.randn((tokens, groups, INDEX_HEADS), generator=gen, device=dev) / 16
+    slots = pool * (block // 8)
+    summaries = torch.empty((slots, groups, INDEX_DIM), dtype=torch.float8_e4m3fn, device=dev)
+    for s0 in range(0, slots, chunk_slots):
+        s1 = min(slots, s0 + chunk_slots)
+        summaries[s0:s1] = _e4m3_normal((s1 - s0, groups, INDEX_DIM), _gen(dev, seed * 7919 + s0), dev)
+    return IndexWorkload(query, weights, summaries, torch.as_tensor(table, device=dev),
+                         torch.as_tensor(lengths.astype(np.int32), device=dev), block, query_len,
+                         int(n_cols))
+
+
+def index_host_subset(w: IndexWorkload, requests) -> IndexWorkload:
+    """Host copy of the listed requests (all their tokens and groups), their pages
+    renumbered densely: the oracle's input for sampled rows of a large workload.
+    Row k * G * query_len + i of the subset is row req_k * G * query_len + i."""
+    requests = [int(r) for r in requests]
+    table = w.block_table.cpu().numpy()
+    per_page = w.block // 8
+    used = sorted({int(p) for r in requests for p in table[r] if p >= 0})
+    remap = {p: i for i, p in enumerate(used)}
+    new_table = np.full((len(requests), table.shape[1]), -1, dtype=np.int32)
+    for k, r in enumerate(requests):
+        for c, p in enumerate(table[r]):
+            if p >= 0:
+                new_table[k, c] = remap[int(p)]
+    page_ids = torch.as_tensor(used, dtype=torch.int64, device=w.summaries.device)
+    pages = w.summaries.view(-1, per_page, w.groups, INDEX_DIM)[page_ids]
+    toks = torch.as_tensor([r * w.query_len + i for r in requests for i in range(w.query_len)],
+                           device=w.query.device)
+    return IndexWorkload(w.query[toks].cpu(), w.weights[toks].cpu(),
+                         pages.reshape(-1, w.groups, INDEX_DIM).cpu(), torch.as_tensor(new_table),
+                         w.seq_lens.cpu()[torch.as_tensor(requests)], w.block, w.query_len, w.n_cols)

@@ -194,3 +194,44 @@ def test_select_entry_validation(lib):
     assert call(lengths=f.t(1, (8,))) == INV
     z = f.t(6, (0, 100))
     assert call(scores=z, current=f.t(4, (0,)), lengths=None, regions=f.t(4, (0, 16))) == B.SDA_OK
+
+
+def test_summary_entry_validation(lib):
+    INV, UNS, WS = B.SDA_ERR_INVALID, B.SDA_ERR_UNSUPPORTED, B.SDA_ERR_WORKSPACE
+    f = FakeDev()
+    r = ctypes.byref
+    T, G = 8, 2
+    q, w = f.t(2, (T, G, 8, 256)), f.t(6, (T, G, 8))
+    m, bt, sl = f.t(3, (100, G, 256)), f.t(4, (4, 16)), f.t(4, (4,))
+    sc, cur, ln = f.t(6, (T * G, 128)), f.t(4, (T * G,)), f.t(4, (T * G,))
+
+    def call(query=q, weights=w, summ=m, table=bt, seq=sl, block=16, ql=2, scores=sc, current=cur,
+             lengths=ln, ws=None, wsb=0):
+        return lib.sparse_decode_summary_scores(r(query), r(weights), r(summ), r(table), r(seq), block, ql,
+                                                r(scores), r(current) if current else None,
+                                                r(lengths) if lengths else None, ws, wsb, None)
+    assert call(block=12) == INV                                # block not a multiple of 8
+    assert call(ql=0) == INV
+    assert call(ql=3) == INV                                    # tokens not a multiple of query_len
+    assert call(query=f.t(2, (T, G, 16, 256))) == INV           # 8 index heads
+    assert call(query=f.t(2, (T, G, 8, 128))) == INV            # 256 dims
+    assert call(query=f.t(1, (T, G, 8, 256))) == INV            # FP8 bytes only
+    assert call(query=f.t(2, (T, G, 8, 256), (G * 4096, 4096, 512, 1))) == INV   # head stride
+    assert call(weights=f.t(6, (T, G, 4))) == INV
+    assert call(weights=f.t(1, (T, G, 8))) == INV
+    assert call(summ=f.t(3, (100, G + 1, 256))) == INV          # groups mismatch
+    assert call(summ=f.t(3, (100, G, 256), (G * 256 + 8, 256, 1))) == UNS       # slot stride
+    assert call(table=f.t(4, (3, 16))) == INV                   # fewer table rows than requests
+    assert call(seq=f.t(4, (3,))) == INV
+    assert call(scores=f.t(6, (T * G - 1, 128))) == INV
+    assert call(scores=f.t(6, (T * G, 128), (256, 2))) == INV   # inner stride
+    assert call(current=f.t(4, (T * G - 1,))) == INV
+    assert call(lengths=f.t(1, (T * G,))) == INV
+    assert call(ws=(1 << 24) + 16, wsb=4096) == WS             # misaligned workspace
+    assert call(ws=1 << 24, wsb=128) == WS                     # too small
+    assert call(query=f.t(2, (T, 1, 8, 256)), weights=f.t(6, (T, 1, 8)), summ=f.t(3, (100, 1, 256)),
+                scores=f.t(6, (T, 128)), current=None, lengths=None, ql=8, table=f.t(4, (1, 16)),
+                seq=f.t(4, (1,))) == UNS                        # query_len > 4
+    z = dict(query=f.t(2, (0, G, 8, 256)), weights=f.t(6, (0, G, 8)), scores=f.t(6, (0, 128)),
+             current=f.t(4, (0,)), lengths=f.t(4, (0,)))
+    assert call(**z) == B.SDA_OK                                # no tokens: nothing to do

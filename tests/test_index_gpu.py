@@ -1,0 +1,190 @@
+"""Indexer decode scores (CUDA kernel vs the oracle), and the whole decode chain
+scores -> region selection -> sparse attention.
+
+Tolerance.  Both sides decode the same E4M3 bytes exactly; each product of two
+E4M3 values is exact in fp32.  The GPU accumulates the 256-term dot products in
+fp32 (the MMA's adds may truncate: at most 2^-23 relative each), then weights
+and sums 8 heads in fp32, so |gpu - oracle| <= (256 + 8) * 2^-23 * A with
+A = sum_h |w_h| sum_d |q_hd| |m_jd|.  The tests use TOL_REL = 4e-5 >= 264 *
+2^-23 of A, with A computed by the oracle on the absolute values (clearing the
+E4M3 sign bits and taking |w|).  The -inf pattern, `current` and `lengths` are
+compared exactly."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_decode_attention_02_gb300 as sda
+from sparse_decode_attention_02_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+TOL_REL = 4e-5
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def run_gpu(w, *, query=None, weights=None, table=None, workspace=None, n_cols=None):
+    n_cols = w.n_cols if n_cols is None else n_cols
+    scores = torch.full((w.rows, n_cols), float("nan"), device=DEV)
+    cur = torch.full((w.rows,), -7, dtype=torch.int32, device=DEV)
+    lens = torch.full((w.rows,), -7, dtype=torch.int32, device=DEV)
+    sda.sparse_decode_summary_scores(w.query if query is None else query,
+                                     w.weights if weights is None else weights, w.summaries,
+                                     w.block_table if table is None else table, w.seq_lens,
+                                     block_size=w.block, query_len=w.query_len, scores=scores,
+                                     current=cur, lengths=lens, workspace=workspace)
+    torch.cuda.synchronize()
+    return scores.cpu().numpy(), cur.cpu().numpy(), lens.cpu().numpy()
+
+
+def run_oracle(h, *, n_cols=None, absolute=False):
+    """The oracle on host workload `h`; with `absolute`, on |q|, |w|, |m| (the error scale)."""
+    q, w, m = h.query.view(torch.uint8), h.weights, h.summaries.view(torch.uint8)
+    if absolute:
+        q, w, m = q & 0x7F, w.abs(), m & 0x7F
+    return oracle.summary_scores(q, w, m, h.block_table, h.seq_lens, block=h.block,
+                                 n_cols=h.n_cols if n_cols is None else n_cols, query_len=h.query_len)
+
+
+def host(w):
+    return inputs.IndexWorkload(w.query.cpu(), w.weights.cpu(), w.summaries.cpu(), w.block_table.cpu(),
+                                w.seq_lens.cpu(), w.block, w.query_len, w.n_cols)
+
+
+def check(got, ref, scale):
+    gs, gc_, gl = got
+    rs, rc, rl = ref
+    assert np.array_equal(gc_, rc) and np.array_equal(gl, rl)
+    assert not np.isnan(gs).any()
+    assert np.array_equal(np.isneginf(gs), np.isneginf(rs))
+    fin = np.isfinite(rs)
+    assert np.isfinite(gs[fin]).all()
+    err = np.abs(gs[fin] - rs[fin])
+    bound = TOL_REL * scale[fin] + 1e-6
+    assert (err <= bound).all(), float(np.max(err / bound))
+
+
+CASES = {
+    "block8_g1": dict(requests=3, groups=1, query_len=1, ctx=(1, 700), block=8),
+    "chunks_g2_ql2": dict(requests=5, groups=2, query_len=2, ctx=(100, 9000), block=16),
+    "g4_ql1": dict(requests=4, groups=4, query_len=1, ctx=(4000, 20000), block=64),
+    "g8_ql3_capped": dict(requests=3, groups=8, query_len=3, ctx=(10, 5000), block=64, n_cols=300),
+    "short_ql4": dict(requests=4, groups=2, query_len=4, ctx=(1, 3), block=16),
+    "g4_ql4_long": dict(requests=2, groups=4, query_len=4, ctx=(30000, 40000), block=32),
+    "g2_ql1_ragged": dict(requests=7, groups=2, query_len=1, ctx=(511 * 8, 513 * 8 + 7), block=64),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_summary_scores_match_oracle(name):
+    w = inputs.make_index_workload(DEV, seed=11, **CASES[name])
+    h = host(w)
+    got = run_gpu(w)
+    check(got, run_oracle(h), run_oracle(h, absolute=True)[0])
+
+
+def test_group_major_strides():
+    """Indexer outputs may be group-major: queries and weights as [G, tokens] views."""
+    w = inputs.make_index_workload(DEV, requests=4, groups=4, query_len=2, ctx=(900, 4000), block=64, seed=5)
+    qg = w.query.permute(1, 0, 2, 3).contiguous().permute(1, 0, 2, 3)
+    wg = w.weights.permute(1, 0, 2).contiguous().permute(1, 0, 2)
+    assert qg.stride(1) > qg.stride(0) and wg.stride(1) > wg.stride(0)
+    h = host(w)
+    check(run_gpu(w, query=qg, weights=wg), run_oracle(h), run_oracle(h, absolute=True)[0])
+
+
+def test_bad_page_flags_and_scores_minus_inf():
+    w = inputs.make_index_workload(DEV, requests=3, groups=2, query_len=1, ctx=(2000, 3000), block=16, seed=9)
+    h = host(w)
+    ref = run_oracle(h)
+    scale = run_oracle(h, absolute=True)[0]
+    bad = w.block_table.clone()
+    bad[1, 3] = w.summaries.shape[0] // 2          # page ids start past the summary buffer
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    got = run_gpu(w, table=bad, workspace=ws)
+    assert sda.read_errors(ws) & sda.FLAG_BOUNDS
+    rows = [2, 3]                                   # request 1's rows (G = 2)
+    cols = slice(3 * 2, 4 * 2)                      # column 3 of 16-token pages = regions 6, 7
+    assert np.all(got[0][rows, cols] == -np.inf)
+    keep = np.ones_like(ref[0], dtype=bool)
+    keep[rows, cols] = False
+    gs = np.where(keep, got[0], ref[0])
+    check((gs, got[1], got[2]), ref, scale)
+    ws.zero_()
+    run_gpu(w, workspace=ws)
+    assert sda.read_errors(ws) == 0
+
+
+def test_no_columns_still_writes_current_and_lengths():
+    w = inputs.make_index_workload(DEV, requests=2, groups=2, query_len=2, ctx=(50, 90), block=16, seed=1)
+    s, c, l = run_gpu(w, n_cols=0)
+    _, rc, rl = run_oracle(host(w), n_cols=0)
+    assert s.shape == (w.rows, 0) and np.array_equal(c, rc) and np.array_equal(l, rl)
+
+
+def test_full_size_sampled_rows():
+    """The decode-row workload at full size (512 requests x 4 groups, contexts
+    128K-256K, 32K columns): sampled requests against the oracle, and the
+    -inf / current / lengths pattern of every row."""
+    w = inputs.make_index_workload(DEV)
+    got = run_gpu(w)
+    seq = w.seq_lens.cpu().numpy().astype(np.int64)
+    pos = np.repeat(seq - 1, w.groups)
+    n = np.minimum(pos // 8 + 1, w.n_cols)
+    assert np.array_equal(got[1], pos // 8) and np.array_equal(got[2], n)
+    cols = np.arange(w.n_cols)
+    assert np.array_equal(np.isneginf(got[0]), cols[None, :] >= n[:, None])
+    assert np.isfinite(got[0][cols[None, :] < n[:, None]]).all()
+    reqs = [0, 217, 511]
+    sub = inputs.index_host_subset(w, reqs)
+    rows = [r * w.groups + g for r in reqs for g in range(w.groups)]
+    check(tuple(x[rows] for x in got), run_oracle(sub), run_oracle(sub, absolute=True)[0])
+
+
+def test_decode_chain_scores_select_attention():
+    """scores -> select_regions -> sparse_decode_attention with 8-token regions,
+    every step on the GPU; each step checked against the oracle on the previous
+    step's GPU output (scores within tolerance, ids exactly, attention within
+    the bf16 tolerance)."""
+    w = inputs.make_index_workload(DEV, requests=6, groups=2, query_len=2, ctx=(3000, 12000), block=64, seed=4)
+    h = host(w)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    scores = torch.empty((w.rows, w.n_cols), device=DEV)
+    cur = torch.empty(w.rows, dtype=torch.int32, device=DEV)
+    lens = torch.empty(w.rows, dtype=torch.int32, device=DEV)
+    sda.sparse_decode_summary_scores(w.query, w.weights, w.summaries, w.block_table, w.seq_lens,
+                                     block_size=w.block, query_len=w.query_len, scores=scores,
+                                     current=cur, lengths=lens, workspace=ws)
+    topk = 64
+    regions = sda.sparse_decode_select_regions(scores, cur, topk, topk_lengths=lens)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    pages = w.summaries.shape[0] // (w.block // 8)
+    cache = torch.randn((pages, w.groups, w.block, 384), generator=g, device=DEV).to(torch.bfloat16)
+    query = torch.randn((w.rows, 16, 192), generator=g, device=DEV).to(torch.bfloat16)
+    seq = w.seq_lens.long()
+    tok = torch.arange(w.tokens, device=DEV)
+    positions = (seq[tok // w.query_len] - w.query_len + tok % w.query_len).repeat_interleave(w.groups)
+    positions = positions.to(torch.int32)
+    active = torch.ones(w.rows, dtype=torch.bool, device=DEV)
+    out = torch.empty_like(query)
+    sda.sparse_decode_attention(query, cache, regions, w.block_table, positions, active, out,
+                                scale=192 ** -0.5, query_len=w.query_len, region_tokens=8)
+    torch.cuda.synchronize()
+    assert sda.read_errors(ws) == 0
+    check((scores.cpu().numpy(), cur.cpu().numpy(), lens.cpu().numpy()), run_oracle(h),
+          run_oracle(h, absolute=True)[0])
+    ref_ids = oracle.select_regions(scores.cpu(), cur.cpu(), topk, lens.cpu())
+    assert np.array_equal(regions.cpu().numpy(), ref_ids)
+    ref = oracle.sparse_decode_attention(query.cpu(), cache.cpu(), regions.cpu(), w.block_table.cpu(),
+                                         positions.cpu(), active.cpu(), scale=192 ** -0.5,
+                                         query_len=w.query_len, region_tokens=8)
+    err = np.abs(out.float().cpu().numpy() - ref).max()
+    assert err <= 2e-2, err
