@@ -13,8 +13,11 @@
 // with row = (token, g), pos the token's position and m_j the summary of
 // region j of group g, found through the request's block-table row.
 //
-// Design.  A CTA takes one (request, group, chunk of 512 regions); its four
-// warps each stream 128 regions as 16-region tiles.  A tile (16 x 256 FP8
+// Design.  A CTA takes one request and a chunk of its regions for a block of
+// up to 4 KV groups, one warp per group (the groups' summaries of a slot are
+// adjacent, so the CTA reads them as one run); with fewer groups per block the
+// spare warps split the chunk.  Each warp streams 1024 regions of its group as
+// 16-region tiles.  A tile (16 x 256 FP8
 // bytes, 4 KB) is copied with 16-byte cp.async into a 4-stage ring of the
 // warp's own shared memory, XOR-swizzled per row so that ldmatrix reads are
 // conflict-free.  The product is an MMA with the regions as M (16) and the 8
@@ -42,12 +45,13 @@ constexpr int kRegionTokens = 8;
 constexpr int kIdxWarps = 4;
 constexpr int kIdxThreads = kIdxWarps * 32;
 constexpr int kTile = 16;             // regions per tile (the MMA's M)
-constexpr int kTilesPerWarp = 8;
+constexpr int kTilesPerWarp = 64;
 constexpr int kStages = 4;            // tiles in a warp's ring
-constexpr int kChunk = kIdxWarps * kTilesPerWarp * kTile;   // regions per CTA
+constexpr int kWarpRegions = kTilesPerWarp * kTile;   // regions one warp streams
 constexpr int kTileBytes = kTile * kIdxDim;
 constexpr int kSmemBytes = kIdxWarps * kStages * kTileBytes;
 constexpr int kMaxQueryLen = 4;
+static_assert(kStages * kTile <= 64, "the ring's row masks are packed into one 64-bit word");
 
 struct IndexParams {
     const uint8_t *query;     // [tokens, G, 8, 256]
@@ -68,7 +72,8 @@ struct IndexParams {
     int32_t *lengths;         // [tokens * G] or NULL
     int64_t len_s0;
     uint32_t *flags;          // workspace header or NULL
-    int groups, block, n_cols, chunks;
+    int groups, block, n_cols;
+    int chunks;               // CTAs per (request, group block)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -125,11 +130,12 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int seg)
     return static_cast<uint32_t>(row * kIdxDim + ((seg ^ (row & 7)) << 4));
 }
 
-// QL = tokens per request.  Each lane keeps, per token and 32-dim chunk kc,
+// QL = tokens per request, GB = groups per CTA (4, 2 or 1, dividing G; the
+// 4 / GB warps of a group split the CTA's regions).  Each lane keeps, per token and 32-dim chunk kc,
 // the query words w0 = bytes [32kc + 4t, +4) and w1 = bytes [32kc + 16 + 4t,
 // +4) of head `gid` (lane = 4 gid + t).  For QL <= 2 they are held already
 // converted to fp16 pairs.
-template <int QL>
+template <int QL, int GB>
 __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -140,8 +146,11 @@ __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexPa
     const int64_t unit = blockIdx.x;
     const int chunk = static_cast<int>(unit % p.chunks);
     const int64_t rest = unit / p.chunks;
-    const int g = static_cast<int>(rest % p.groups);
-    const int64_t req = rest / p.groups;
+    constexpr int kChunkRegions = (kIdxWarps / GB) * kWarpRegions;
+    const int gblocks = p.groups / GB;
+    const int g = static_cast<int>(rest % gblocks) * GB + warp % GB;
+    const int sub = warp / GB;   // this warp's part of the chunk
+    const int64_t req = rest / gblocks;
 
     const int64_t seq_len = p.seq_lens[req * p.sl_s0];
     int n_tok[QL];
@@ -154,7 +163,7 @@ __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexPa
             n = p.n_cols;
         n_tok[i] = static_cast<int>(n);
         n_max = n_tok[i] > n_max ? n_tok[i] : n_max;
-        if (chunk == 0 && warp == 0 && lane == 0) {
+        if (chunk == 0 && sub == 0 && lane == 0) {
             const int64_t row = (req * QL + i) * p.groups + g;
             if (p.current)
                 p.current[row * p.cur_s0] = pos >= 0 ? static_cast<int32_t>(pos / kRegionTokens) : -1;
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexPa
         }
     }
 
-    const int region0 = chunk * kChunk + warp * (kTilesPerWarp * kTile);
+    const int region0 = chunk * kChunkRegions + sub * kWarpRegions;
     int tiles = 0;   // tiles of this warp that hold scored regions
     if (region0 < n_max)
         tiles = min(kTilesPerWarp, (n_max - region0 + kTile - 1) / kTile);
@@ -334,7 +343,7 @@ __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexPa
 cudaError_t ensure_index_smem(const void *kernel, int slot)
 {
     static std::mutex mu;
-    static bool raised[kMaxQueryLen][256] = {};
+    static bool raised[kMaxQueryLen * 3][256] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -418,9 +427,13 @@ extern "C" sda_status sparse_decode_summary_scores(
     // 16-byte copies and 4-byte query loads.
     if (query->stride[0] % 16 || query->stride[1] % 16 || summaries->stride[0] % 16)
         return SDA_ERR_UNSUPPORTED;
-    const int64_t chunks = n_cols > 0 ? (n_cols + kChunk - 1) / kChunk : 1;
-    if (n_cols > INT32_MAX - kChunk || block_table->shape[1] > INT32_MAX || block_size > INT32_MAX / 2 ||
-        chunks * groups * reqs > INT32_MAX)
+    // The warps of a CTA take the same regions of up to 4 groups (their
+    // summaries are adjacent in memory), or split the regions of fewer.
+    const int gblock = groups % 4 == 0 ? 4 : (groups % 2 == 0 ? 2 : 1);
+    const int chunk_regions = (kIdxWarps / gblock) * kWarpRegions;
+    const int64_t chunks = n_cols > 0 ? (n_cols + chunk_regions - 1) / chunk_regions : 1;
+    if (n_cols > INT32_MAX - chunk_regions || block_table->shape[1] > INT32_MAX ||
+        block_size > INT32_MAX / 2 || groups > INT32_MAX || chunks * (groups / gblock) * reqs > INT32_MAX)
         return SDA_ERR_UNSUPPORTED;
     if (rows == 0)
         return SDA_OK;
@@ -457,16 +470,19 @@ extern "C" sda_status sparse_decode_summary_scores(
     prm.n_cols = static_cast<int>(n_cols);
     prm.chunks = static_cast<int>(chunks);
 
-    const void *kernels[kMaxQueryLen] = {
-        reinterpret_cast<const void *>(sda_index_kernel<1>),
-        reinterpret_cast<const void *>(sda_index_kernel<2>),
-        reinterpret_cast<const void *>(sda_index_kernel<3>),
-        reinterpret_cast<const void *>(sda_index_kernel<4>)};
-    const void *kernel = kernels[query_len - 1];
-    if (ensure_index_smem(kernel, query_len - 1) != cudaSuccess)
+#define SDA_INDEX_KERNELS(QL)                                                   \
+    {reinterpret_cast<const void *>(sda_index_kernel<QL, 1>),                   \
+     reinterpret_cast<const void *>(sda_index_kernel<QL, 2>),                   \
+     reinterpret_cast<const void *>(sda_index_kernel<QL, 4>)}
+    const void *kernels[kMaxQueryLen][3] = {SDA_INDEX_KERNELS(1), SDA_INDEX_KERNELS(2),
+                                            SDA_INDEX_KERNELS(3), SDA_INDEX_KERNELS(4)};
+#undef SDA_INDEX_KERNELS
+    const int gb_slot = gblock == 4 ? 2 : gblock - 1;
+    const void *kernel = kernels[query_len - 1][gb_slot];
+    if (ensure_index_smem(kernel, (query_len - 1) * 3 + gb_slot) != cudaSuccess)
         return SDA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(chunks * groups * reqs));
+    cfg.gridDim = dim3(static_cast<unsigned>(chunks * (groups / gblock) * reqs));
     cfg.blockDim = dim3(kIdxThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = static_cast<cudaStream_t>(stream);
