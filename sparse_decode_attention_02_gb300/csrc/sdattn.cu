@@ -203,13 +203,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, int w, uint32_t bar)
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            int c3, int c4, uint32_t bar)
 {
     asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar)
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
         : "memory");
 }
 
@@ -323,6 +323,18 @@ __device__ __forceinline__ int rowmap(int n)
     return (n >> 1) | ((n & 1) << 2);
 }
 
+// A stage holds its pieces of P slots one after another, each stored as
+// [band][row][128 bytes] (one TMA box), so the 8-slot tile starting at slot s
+// (8 | P, 8 | s) sits at this byte offset and its bands are P * 128 bytes
+// apart.  With P = slots per stage this is the plain [band][slot] layout.
+// Tiles past the stage's last piece (P not dividing the stage) alias tile 0:
+// their slots are never valid.
+__device__ __forceinline__ uint32_t tile_offset(int s, int P, int pieces_per_stage, uint32_t piece_stride)
+{
+    const int k = s / P;
+    return k < pieces_per_stage ? k * piece_stride + static_cast<uint32_t>(s - k * P) * 128u : 0u;
+}
+
 // O[16 heads x 192] += P[16 x 16 slots] V[16 slots x 192] for one warp.  V is
 // read with ldmatrix.trans from the stage's V bands: lane `mi = lane / 8`
 // addresses k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of a chunk pair;
@@ -330,7 +342,7 @@ __device__ __forceinline__ int rowmap(int n)
 // V values of invalid slots (vm0: k-slots 2t, 2t+1; vm1: 8+2t, 9+2t).
 template <bool FP8, bool MASKED>
 __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t (&pa)[4], uint32_t vrow,
-                                              int mi, int vsw, uint32_t vm0, uint32_t vm1)
+                                              uint32_t bstride, int mi, int vsw, uint32_t vm0, uint32_t vm1)
 {
     if constexpr (FP8) {
         // 16-dim chunks cv = 0..11: V dims 0..63 sit in band 1 chunks 4..7,
@@ -342,7 +354,7 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
             const int band = cv < 4 ? 1 : 2;
             const int ch = cv < 4 ? cv + 4 : cv - 4;
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vrow + band * Traits<FP8>::kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+            ldsm_x4_trans(vrow + band * bstride + ((ch ^ vsw) << 4), r0, r1, r2, r3);
             if constexpr (MASKED) {
                 r0 &= vm0;
                 r1 &= vm1;
@@ -364,7 +376,7 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
             const int band = 3 + (cv >> 3);
             const int ch = cv & 7;
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vrow + band * Traits<FP8>::kBandBytes + ((ch ^ vsw) << 4), r0, r1, r2, r3);
+            ldsm_x4_trans(vrow + band * bstride + ((ch ^ vsw) << 4), r0, r1, r2, r3);
             if constexpr (MASKED) {
                 r0 &= vm0;
                 r1 &= vm1;
@@ -475,7 +487,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int o = 16; o; o >>= 1)
             pieces += __shfl_xor_sync(~0u, pieces, o);
         if (lane == 0) {
-            ctl[0] = static_cast<int>((pieces * P + T::kSlots - 1) / T::kSlots);
+            const int per_stage = T::kSlots / P;   // P need not divide the stage
+            ctl[0] = static_cast<int>((pieces + per_stage - 1) / per_stage);
             ctl[1] = lo;
             ctl[2] = hi;
         }
@@ -526,75 +539,94 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int grp = row % p.groups;
         const int32_t *bt = p.block_table + req * p.bt_s0;
         const int pps = T::kSlots / P;
-        const uint32_t piece_bytes = static_cast<uint32_t>(P) * kRow * T::kElt;
+        const uint32_t piece_bytes = static_cast<uint32_t>(P) * kRow * T::kElt;   // = one box
         int stage = 0, fill = 0, issued = 0;
         uint32_t phase = 0;
         uint64_t mask = 0;
         bool aborted = false;
-        for (int base = lo; base < hi && !aborted; base += 32) {
-            const int i = base + lane;
-            const bool have_r = i < hi;
-            const int id = have_r ? (windowed ? win_base + i : live[i]) : 0;
-            const int64_t first = static_cast<int64_t>(id) * p.region_tokens;
-            const int pc = have_r ? static_cast<int>(min(static_cast<int64_t>(npr), (pos - first) / P + 1)) : 0;
-            for (int j = 0; j < npr && !aborted; ++j) {
-                const bool have = j < pc;
-                const int64_t t0 = first + static_cast<int64_t>(j) * P;
-                const int64_t col = t0 / p.block;
-                const int off = static_cast<int>(t0 - col * p.block);
-                int page = -1;
-                if (have) {
-                    if (col < p.table_cols)
-                        page = bt[col];
-                    if (col >= p.table_cols || page < 0 || page >= p.pages) {
-                        atomicOr(p.flags, SDA_FLAG_BOUNDS);
-                        page = -1;
-                    }
-                }
-                // valid slots of the piece: [skip, nv) (skip > 0 only for a window's first piece)
-                const int nv = have ? static_cast<int>(min(static_cast<int64_t>(P), pos - t0 + 1)) : 0;
-                const int skip = have ? static_cast<int>(max(static_cast<int64_t>(0), win_lo - t0)) : 0;
-                unsigned bits = __ballot_sync(~0u, have);
-                while (bits) {
-                    const int src = __ffs(bits) - 1;
-                    bits &= bits - 1;
-                    const int pg = __shfl_sync(~0u, page, src);
-                    const int of = __shfl_sync(~0u, off, src);
-                    const int n = __shfl_sync(~0u, nv, src);
-                    const int sk = __shfl_sync(~0u, skip, src);
-                    if (lane == 0 && !aborted) {
-                        if (fill == 0 && issued >= T::kStages &&
-                            !mbar_wait(empty_bar + 8 * stage, phase ^ 1u, p.wait_ns)) {
-                            atomicOr(p.flags, SDA_FLAG_TIMEOUT);
-                            aborted = true;
-                        }
-                        if (!aborted) {
-                            if (pg >= 0) {
-                                const uint32_t fb = full_bar + 8 * stage;
-                                mbar_expect_tx(fb, piece_bytes);
-                                const uint32_t dst = sbase + stage * L::kStageBytes + fill * P * 128;
-#pragma unroll
-                                for (int b = 0; b < T::kBands; ++b)
-                                    tma_load_4d(dst + b * T::kBandBytes, &tmap, b * (128 / T::kElt), of,
-                                                grp, pg, fb);
-                                const uint64_t bitsv = (n >= 64 ? ~0ull : ((1ull << n) - 1ull)) &
-                                                       ~((1ull << sk) - 1ull);
-                                mask |= bitsv << (fill * P);
-                            }
-                            if (++fill == pps) {
-                                hdr[stage] = mask;
-                                mbar_arrive(full_bar + 8 * stage);
-                                ++issued;
-                                fill = 0;
-                                mask = 0;
-                                if (++stage == T::kStages) {
-                                    stage = 0;
-                                    phase ^= 1u;
-                                }
-                            }
-                        }
+        // Candidate pieces c = 0, 1, ... are (live region lo + c / npr, piece
+        // c % npr); the visible ones fill the stages densely, in that order.
+        // Each batch of 32 candidates is resolved one per lane, and the lanes
+        // holding the pieces of a stage issue their copies together.
+        const int n_cand = (hi - lo) * npr;
+        // The next batch's table entries are loaded while this batch issues.
+        bool nx_have = false, nx_col_ok = false;
+        int nx_page = -1, nx_off = 0;
+        int64_t nx_t0 = 0;
+        auto fetch = [&](int b) {
+            const int c = b + lane;
+            nx_have = c < n_cand;
+            const int i = lo + (nx_have ? c / npr : 0);
+            const int j = nx_have ? c % npr : 0;
+            const int id = nx_have ? (windowed ? win_base + i : live[i]) : 0;
+            nx_t0 = static_cast<int64_t>(id) * p.region_tokens + static_cast<int64_t>(j) * P;
+            nx_have = nx_have && nx_t0 <= pos;
+            const int64_t col = nx_t0 / p.block;
+            nx_off = static_cast<int>(nx_t0 - col * p.block);
+            nx_col_ok = col < p.table_cols;
+            nx_page = nx_have && nx_col_ok ? bt[col] : -1;
+        };
+        fetch(0);
+        for (int base = 0; base < n_cand && !aborted; base += 32) {
+            const bool have = nx_have;
+            const int off = nx_off;
+            const int64_t t0 = nx_t0;
+            int page = nx_page;
+            if (have && (!nx_col_ok || page < 0 || page >= p.pages)) {
+                atomicOr(p.flags, SDA_FLAG_BOUNDS);
+                page = -1;
+            }
+            if (base + 32 < n_cand)
+                fetch(base + 32);
+            // valid slots of the piece: [skip, nv) (skip > 0 only for a window's first piece)
+            const int nv = have ? static_cast<int>(min(static_cast<int64_t>(P), pos - t0 + 1)) : 0;
+            const int skip = have ? static_cast<int>(max(static_cast<int64_t>(0), win_lo - t0)) : 0;
+            const uint64_t pbits = (nv >= 64 ? ~0ull : ((1ull << nv) - 1ull)) & ~((1ull << skip) - 1ull);
+            const unsigned hv = __ballot_sync(~0u, have);
+            const int rank = __popc(hv & ((1u << lane) - 1u));
+            const int nh = __popc(hv);
+            for (int done = 0; done < nh;) {
+                if (fill == 0 && issued >= T::kStages) {
+                    if (lane == 0 && !mbar_wait(empty_bar + 8 * stage, phase ^ 1u, p.wait_ns)) {
+                        atomicOr(p.flags, SDA_FLAG_TIMEOUT);
+                        aborted = true;
                     }
                     aborted = __shfl_sync(~0u, aborted, 0);
+                    if (aborted)
+                        break;
+                }
+                const int take = min(pps - fill, nh - done);
+                const bool mine = have && rank >= done && rank < done + take;
+                const bool copy = mine && page >= 0;
+                const unsigned cb = __ballot_sync(~0u, copy);
+                const uint32_t fb = full_bar + 8 * stage;
+                if (lane == 0 && cb)
+                    mbar_expect_tx(fb, __popc(cb) * piece_bytes);
+                __syncwarp();
+                uint64_t mbits = 0;
+                if (copy) {
+                    const int slot = fill + rank - done;
+                    tma_load_5d(sbase + stage * L::kStageBytes + slot * piece_bytes, &tmap, 0, off, 0, grp,
+                                page, fb);
+                    mbits = pbits << (slot * P);
+                }
+                const unsigned lo32 = __reduce_or_sync(~0u, static_cast<unsigned>(mbits));
+                const unsigned hi32 = __reduce_or_sync(~0u, static_cast<unsigned>(mbits >> 32));
+                mask |= (static_cast<uint64_t>(hi32) << 32) | lo32;
+                fill += take;
+                done += take;
+                if (fill == pps) {
+                    if (lane == 0) {
+                        hdr[stage] = mask;
+                        mbar_arrive(fb);
+                    }
+                    ++issued;
+                    fill = 0;
+                    mask = 0;
+                    if (++stage == T::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
         }
@@ -637,9 +669,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     // k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of the chunk pair.
     const int mi = lane >> 3;
     const int vk = (mi & 1) * 8 + (lane & 7);
-    const int vslot = slot0 + (vk & 8) + rowmap(vk & 7);
-    const int vsw = vslot & 7;
+    const int vsw = rowmap(vk & 7);        // swizzle phase of this lane's V rows
     const int sw = rowmap(g);              // swizzle phase of this lane's K rows
+    // Stage offsets of this warp's K tile rows and V k-step rows, and the band stride.
+    const int pps_c = T::kSlots / p.piece;
+    const uint32_t bstride = static_cast<uint32_t>(p.piece) * 128u;
+    const uint32_t pstride = bstride * T::kBands;
+    uint32_t krow[NT], vrow_off[KS];
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+        krow[i] = tile_offset(slot0 + 8 * i, p.piece, pps_c, pstride) + sw * 128u;
+#pragma unroll
+    for (int k2 = 0; k2 < KS; ++k2)
+        vrow_off[k2] = tile_offset(slot0 + 16 * k2 + (vk & 8), p.piece, pps_c, pstride) + vsw * 128u;
 
     for (int st = pair; st < n_st; st += kPairs) {
         const int s = st % T::kStages;
@@ -659,7 +701,6 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int i = 0; i < NT; ++i)
                 sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.0f;
-            const uint32_t row0 = stage_base + (slot0 + sw) * 128;
             if constexpr (FP8) {
                 // thread t: band 0 chunks t and t+4, band 1 chunk t (16 dims each);
                 // tiles in pairs to bound the live K words.
@@ -669,9 +710,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                     for (int c = 0; c < 3; ++c) {
                         const int band = c == 2 ? 1 : 0;
                         const int ch = c == 1 ? t + 4 : t;
-                        const uint32_t off = band * T::kBandBytes + ((ch ^ sw) << 4);
-                        const uint4 ka = lds128(row0 + i0 * 8 * 128 + off);
-                        const uint4 kb = lds128(row0 + (i0 + 1) * 8 * 128 + off);
+                        const uint32_t off = band * bstride + ((ch ^ sw) << 4);
+                        const uint4 ka = lds128(stage_base + krow[i0] + off);
+                        const uint4 kb = lds128(stage_base + krow[i0 + 1] + off);
                         const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w};
                         const uint32_t wb[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
@@ -689,11 +730,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int j = 0; j < 6; ++j) {
                     const int band = j >> 1;
                     const int ch = (j & 1) * 4 + t;
-                    const uint32_t off = band * T::kBandBytes + ((ch ^ sw) << 4);
+                    const uint32_t off = band * bstride + ((ch ^ sw) << 4);
                     uint4 kv[NT];
 #pragma unroll
                     for (int i = 0; i < NT; ++i)
-                        kv[i] = lds128(row0 + i * 8 * 128 + off);
+                        kv[i] = lds128(stage_base + krow[i] + off);
                     const uint4 qa = lds128(qfrag + ((2 * j) * 32 + lane) * 16);
                     const uint4 qb = lds128(qfrag + ((2 * j + 1) * 32 + lane) * 16);
                     const uint32_t qfa[4] = {qa.x, qa.y, qa.z, qa.w};
@@ -769,15 +810,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int k2 = 0; k2 < KS; ++k2) {
                 const uint32_t km = (wm >> (16 * k2)) & 0xFFFFu;
-                const uint32_t vrow = stage_base + (vslot + 16 * k2) * 128;
+                const uint32_t vrow = stage_base + vrow_off[k2];
                 if (km == 0xFFFFu) {
-                    pv_accumulate<FP8, false>(o, pa[k2], vrow, mi, vsw, 0u, 0u);
+                    pv_accumulate<FP8, false>(o, pa[k2], vrow, bstride, mi, vsw, 0u, 0u);
                 } else if (km) {
                     const uint32_t vm0 = (((km >> t) & 1u) ? 0x0000FFFFu : 0u) |
                                          (((km >> (t + 4)) & 1u) ? 0xFFFF0000u : 0u);
                     const uint32_t vm1 = (((km >> (t + 8)) & 1u) ? 0x0000FFFFu : 0u) |
                                          (((km >> (t + 12)) & 1u) ? 0xFFFF0000u : 0u);
-                    pv_accumulate<FP8, true>(o, pa[k2], vrow, mi, vsw, vm0, vm1);
+                    pv_accumulate<FP8, true>(o, pa[k2], vrow, bstride, mi, vsw, vm0, vm1);
                 }
             }
         }
@@ -1202,20 +1243,24 @@ sda_status run_call(const Call &c)
     if (windowed ? !c.seq_lens->data : (!c.regions->data || !c.positions->data || !c.active->data))
         return SDA_ERR_INVALID;
 
-    // ---- Tensor map over the whole cache: dims (384, B, G, pages), boxes of
-    // 128 bytes x P tokens, 128-byte swizzle.
+    // ---- Tensor map over the whole cache as (128-byte band chunk, token, band,
+    // group, page): one box of 128 bytes x P tokens x all bands is a whole
+    // piece, landing as [band][token][128 bytes] with 128-byte swizzle.
     EncodeTiledFn encode = encode_fn();
     if (!encode)
         return SDA_ERR_CUDA;
     CUtensorMap tmap;
-    const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(block),
-                                static_cast<cuuint64_t>(groups), static_cast<cuuint64_t>(pages)};
-    const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(cache->stride[2] * elt),
+    const int bands = kRow * elt / 128;
+    const cuuint64_t gdim[5] = {static_cast<cuuint64_t>(128 / elt), static_cast<cuuint64_t>(block),
+                                static_cast<cuuint64_t>(bands), static_cast<cuuint64_t>(groups),
+                                static_cast<cuuint64_t>(pages)};
+    const cuuint64_t gstride[4] = {static_cast<cuuint64_t>(cache->stride[2] * elt), 128u,
                                    static_cast<cuuint64_t>(cache->stride[1] * elt),
                                    static_cast<cuuint64_t>(cache->stride[0] * elt)};
-    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(piece), 1, 1};
-    const cuuint32_t estride[4] = {1, 1, 1, 1};
-    if (encode(&tmap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+    const cuuint32_t box[5] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(piece),
+                               static_cast<cuuint32_t>(bands), 1, 1};
+    const cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    if (encode(&tmap, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
                const_cast<void *>(cache->data), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

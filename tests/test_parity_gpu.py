@@ -128,6 +128,7 @@ def test_variants(changes, fp8):
     dict(block=128, region_tokens=128, num_regions=12),             # a region = 2 FP8 / 4 bf16 pieces
     dict(block=32, region_tokens=64, num_regions=20, query_len=2),  # a region spans two blocks
     dict(block=64, region_tokens=16, num_regions=150, heads=12),    # four regions per page
+    dict(block=24, region_tokens=24, num_regions=40),               # pieces that do not divide a stage
 ])
 @pytest.mark.parametrize("fp8", [False, True])
 def test_more_layouts(changes, fp8):
@@ -135,6 +136,17 @@ def test_more_layouts(changes, fp8):
     rows = list(range(w.rows))
     ref = oracle_rows(w, rows)
     for s in (1, 3):
+        out, flags = run(w, splits=s)
+        assert flags == 0
+        check(w, out, ref, rows)
+
+
+def test_fp8_pages_of_48_tokens():
+    """One 48-token piece per 64-slot FP8 stage."""
+    w = mini("fp8", requests=4, ctx=(2000, 6000), block=48, region_tokens=48, num_regions=24)
+    rows = list(range(w.rows))
+    ref = oracle_rows(w, rows)
+    for s in (1, 2):
         out, flags = run(w, splits=s)
         assert flags == 0
         check(w, out, ref, rows)

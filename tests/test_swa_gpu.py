@@ -56,6 +56,8 @@ def test_swa_windows(window, fp8):
     dict(query_len=3, groups=2, heads=5),
     dict(query_len=4, groups=4, heads=16, block=16),
     dict(query_len=2, groups=2, heads=8, block=32, gate=False),
+    dict(query_len=2, groups=2, heads=8, block=24),                 # 24-token pieces
+    dict(query_len=1, groups=2, heads=4, block=48, fp8=True),       # one 48-token piece per stage
 ])
 def test_swa_shapes(changes):
     w = mini(requests=4, ctx=(900, 3000), window=513, **changes)
