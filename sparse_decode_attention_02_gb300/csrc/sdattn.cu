@@ -393,7 +393,9 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
 // Split kernel
 // ---------------------------------------------------------------------------
 
-template <bool FP8, bool WINDOW>
+// FULL: a piece fills a whole stage (P = slots per stage), so the stage
+// layout is a compile-time [band][slot] one.
+template <bool FP8, bool WINDOW, bool FULL>
 __global__ void __launch_bounds__(kThreads, 2)
     sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
 {
@@ -672,16 +674,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int vsw = rowmap(vk & 7);        // swizzle phase of this lane's V rows
     const int sw = rowmap(g);              // swizzle phase of this lane's K rows
     // Stage offsets of this warp's K tile rows and V k-step rows, and the band stride.
-    const int pps_c = T::kSlots / p.piece;
-    const uint32_t bstride = static_cast<uint32_t>(p.piece) * 128u;
+    const int piece_c = FULL ? T::kSlots : p.piece;
+    const int pps_c = T::kSlots / piece_c;
+    const uint32_t bstride = static_cast<uint32_t>(piece_c) * 128u;
     const uint32_t pstride = bstride * T::kBands;
     uint32_t krow[NT], vrow_off[KS];
 #pragma unroll
     for (int i = 0; i < NT; ++i)
-        krow[i] = tile_offset(slot0 + 8 * i, p.piece, pps_c, pstride) + sw * 128u;
+        krow[i] = (FULL ? (slot0 + 8 * i) * 128u : tile_offset(slot0 + 8 * i, piece_c, pps_c, pstride)) +
+                  sw * 128u;
 #pragma unroll
     for (int k2 = 0; k2 < KS; ++k2)
-        vrow_off[k2] = tile_offset(slot0 + 16 * k2 + (vk & 8), p.piece, pps_c, pstride) + vsw * 128u;
+        vrow_off[k2] = (FULL ? (slot0 + 16 * k2 + (vk & 8)) * 128u
+                             : tile_offset(slot0 + 16 * k2 + (vk & 8), piece_c, pps_c, pstride)) +
+                       vsw * 128u;
 
     for (int st = pair; st < n_st; st += kPairs) {
         const int s = st % T::kStages;
@@ -1015,7 +1021,7 @@ bool dims_ok(const sda_tensor *t, int ndim)
 
 // The dynamic shared memory limit each kernel instantiation has been raised to,
 // per device.
-template <bool FP8, bool WINDOW>
+template <bool FP8, bool WINDOW, bool FULL>
 cudaError_t ensure_smem(size_t bytes)
 {
     static std::mutex mu;
@@ -1028,20 +1034,20 @@ cudaError_t ensure_smem(size_t bytes)
     size_t &cur = raised[dev & 63];
     if (bytes <= cur)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(sda_split_kernel<FP8, WINDOW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sda_split_kernel<FP8, WINDOW, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes));
     if (e == cudaSuccess)
         cur = bytes;
     return e;
 }
 
-template <bool FP8, bool WINDOW>
+template <bool FP8, bool WINDOW, bool FULL>
 sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, cudaStream_t stream)
 {
     const size_t smem = Layout<FP8>::bytes(num_regions);
     if (smem > 227 * 1024)
         return SDA_ERR_UNSUPPORTED;
-    if (ensure_smem<FP8, WINDOW>(smem) != cudaSuccess)
+    if (ensure_smem<FP8, WINDOW, FULL>(smem) != cudaSuccess)
         return SDA_ERR_CUDA;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1053,7 +1059,7 @@ sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, c
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8, WINDOW>, tmap, prm) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8, WINDOW, FULL>, tmap, prm) != cudaSuccess)
         return SDA_ERR_CUDA;
     if (prm.splits > 1) {
         cudaLaunchConfig_t c2 = {};
@@ -1315,10 +1321,16 @@ sda_status run_call(const Call &c)
     prm.clear_inactive = c.clear_inactive ? 1 : 0;
 
     cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+    const int nr = windowed ? 0 : prm.num_regions;
+    const bool full = piece == stage_tokens;
+    if (fp8) {
+        if (windowed)
+            return full ? launch<true, true, true>(tmap, prm, nr, s) : launch<true, true, false>(tmap, prm, nr, s);
+        return full ? launch<true, false, true>(tmap, prm, nr, s) : launch<true, false, false>(tmap, prm, nr, s);
+    }
     if (windowed)
-        return fp8 ? launch<true, true>(tmap, prm, 0, s) : launch<false, true>(tmap, prm, 0, s);
-    return fp8 ? launch<true, false>(tmap, prm, prm.num_regions, s)
-               : launch<false, false>(tmap, prm, prm.num_regions, s);
+        return full ? launch<false, true, true>(tmap, prm, nr, s) : launch<false, true, false>(tmap, prm, nr, s);
+    return full ? launch<false, false, true>(tmap, prm, nr, s) : launch<false, false, false>(tmap, prm, nr, s);
 }
 
 }  // namespace
