@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", default="large", choices=inputs.ORDER + ["select"])
+    ap.add_argument("--config", default="large", choices=inputs.ORDER + ["select", "index", "decode"])
     ap.add_argument("--splits", type=int, default=None, help="force a split count")
     ap.add_argument("--requests", type=int, default=None, help="shrink the batch (profiling)")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="context range override (profiling)")
@@ -211,19 +211,19 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def ncu_traffic(cfg_name, alg_bytes):
-    """Per-launch DRAM bytes from the committed ncu capture, scaled by algorithmic
+def ncu_traffic(cfg_name, alg_bytes, record="ncu_traffic.txt", source="sdattn.cu"):
+    """Per-launch DRAM bytes from a committed ncu capture, scaled by algorithmic
     bytes to this launch; None if the capture is for another workload or the
     kernel source changed since it was taken."""
     import hashlib
     try:
         fields = {}
-        with open(os.path.join(ROOT, "profiles", "ncu_traffic.txt")) as f:
+        with open(os.path.join(ROOT, "profiles", record)) as f:
             for line in f:
                 line = line.split("#")[0].split()
                 if len(line) == 2:
                     fields[line[0]] = line[1]
-        src = os.path.join(ROOT, "sparse_decode_attention_02_gb300", "csrc", "sdattn.cu")
+        src = os.path.join(ROOT, "sparse_decode_attention_02_gb300", "csrc", source)
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if sha != fields["kernel_source_sha256_16"] or fields["workload"] != cfg_name:
             return None
@@ -280,6 +280,29 @@ def run_reference(args, world, rank):
             "config": {"workload": "select: 2048 rows, topk 1024", "rows": sw.rows, "topk": sw.topk},
             "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
                              "sample": f"{n} seeded rows per step"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
+    if args.config in ("index", "decode"):
+        dev = "cpu" if not torch.cuda.is_available() else "cuda:0"
+        src = (inputs.make_decode_chain(dev, **index_kw(args)) if args.config == "decode"
+               else inputs.make_index_workload(dev, **index_kw(args)))
+        iw = src.index if args.config == "decode" else src
+        steps = args.steps or 3
+        samples, rows = [], 0
+        for k in range(args.warmup + steps):
+            rows, dt, what = cpu_index_sample(args, args.config, src, k)
+            if k >= args.warmup:
+                samples.append(dt)
+        value = rows * steps / sum(samples)
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC if args.config == "decode" else INDEX_METRIC,
+            "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(samples) / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": index_config(args.config, iw, src.topk if args.config == "decode" else None),
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": what},
             "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
             flush=True)
         return
@@ -370,6 +393,223 @@ def run_select(args, dev, world, rank):
         print(json.dumps(line), flush=True)
 
 
+INDEX_METRIC = ("indexer score rows/s (8-token region summaries, 16K-32K regions per (token, KV group) "
+                "row), 1 GPU")
+DECODE_METRIC = ("DSA decode rows/s: indexer scores + top-1024 selection of 8-token regions + sparse "
+                 "attention over them (FP8 cache), 1 GPU")
+
+
+def index_traffic(iw, with_outputs=False) -> int:
+    """Algorithmic bytes of one indexer launch: every scored region's summary once
+    per (request, group), the score matrix, queries, weights, table entries."""
+    seq = iw.seq_lens.cpu().numpy().astype(np.int64)
+    n = np.minimum((seq - 1) // 8 + 1, iw.n_cols)
+    n = np.where(seq >= 1, n, 0)
+    pages = -(-n * 8 // iw.block)
+    b = int(n.sum()) * iw.groups * inputs.INDEX_DIM
+    b += iw.rows * iw.n_cols * 4
+    b += iw.tokens * iw.groups * inputs.INDEX_HEADS * (inputs.INDEX_DIM + 4)
+    b += int(pages.sum()) * 4 + len(seq) * 4
+    if with_outputs:
+        b += iw.rows * 8                                 # current, lengths
+    return b
+
+
+def chain_host_subset(ch, requests):
+    """Host copies of the listed requests for the oracle chain: indexer inputs,
+    the requests' cache pages (renumbered like the summaries), attention rows."""
+    iw = ch.index
+    sub = inputs.index_host_subset(iw, requests)
+    table = iw.block_table.cpu().numpy()
+    used = sorted({int(p) for r in requests for p in table[r] if p >= 0})
+    cache = ch.cache[torch.as_tensor(used, dtype=torch.int64, device=ch.cache.device)].cpu()
+    per = iw.groups * iw.query_len
+    rows = torch.as_tensor([r * per + i for r in requests for i in range(per)])
+    return sub, cache, ch.query.cpu()[rows], ch.positions.cpu()[rows], ch.active.cpu()[rows]
+
+
+def oracle_chain(ch, sub, cache, query, positions, active):
+    import oracle
+    iw = ch.index
+    sc, cur, ln = oracle.summary_scores(sub.query, sub.weights, sub.summaries, sub.block_table,
+                                        sub.seq_lens, block=iw.block, n_cols=iw.n_cols,
+                                        query_len=iw.query_len)
+    regions = oracle.select_regions(sc.astype(np.float32), cur, ch.topk, ln)
+    return oracle.sparse_decode_attention(query, cache, regions, sub.block_table, positions, active,
+                                          scale=ch.scale, query_len=iw.query_len, region_tokens=8,
+                                          k_scale=ch.k_scale, v_scale=ch.v_scale, cache_fp8=True)
+
+
+def cpu_index_sample(args, kind, src, k=0):
+    """One bounded oracle sample: (rows, seconds, description)."""
+    import oracle
+    iw = src.index if kind == "decode" else src
+    n_req = args.cpu_rows or (1 if kind == "decode" else 2)
+    reqs = sorted(np.random.default_rng(2000 + k).choice(iw.seq_lens.shape[0], size=n_req, replace=False))
+    if kind == "decode":
+        hs = chain_host_subset(src, reqs)
+        t0 = time.perf_counter()
+        oracle_chain(src, *hs)
+    else:
+        sub = inputs.index_host_subset(iw, reqs)
+        t0 = time.perf_counter()
+        oracle.summary_scores(sub.query, sub.weights, sub.summaries, sub.block_table, sub.seq_lens,
+                              block=iw.block, n_cols=iw.n_cols, query_len=iw.query_len)
+    dt = time.perf_counter() - t0
+    rows = n_req * iw.groups * iw.query_len
+    return rows, dt, f"{rows} rows of {n_req} seeded request(s) per sample"
+
+
+def index_config(kind, iw, topk=None):
+    lo, hi = int(iw.seq_lens.min()), int(iw.seq_lens.max())
+    c = {"workload": (f"{kind}: {iw.seq_lens.shape[0]} requests x {iw.groups} KV groups x query_len "
+                      f"{iw.query_len}, contexts {lo}-{hi}, {iw.block}-token pages, 8-token regions, "
+                      f"{iw.n_cols} score columns, 8 index heads x 256 FP8"),
+         "rows": iw.rows, "requests": int(iw.seq_lens.shape[0]), "groups": iw.groups,
+         "query_len": iw.query_len, "score_columns": iw.n_cols,
+         "l2": "inputs larger than L2 (summaries per step >> 129 MB)"}
+    if topk:
+        c["topk"] = topk
+        c["workload"] += f", top-{topk} regions -> FP8 attention, 16 heads x 192"
+    return c
+
+
+def index_kw(args) -> dict:
+    kw = {}
+    if args.requests:
+        kw["requests"] = args.requests
+    if args.ctx:
+        kw["ctx"] = tuple(args.ctx)
+    return kw
+
+
+def run_index(args, dev, world, rank, kind):
+    """The indexer alone (`index`), or a whole DSA decode step (`decode`):
+    indexer scores -> region selection -> sparse attention over 8-token regions."""
+    import sparse_decode_attention_02_gb300 as sda
+    if kind == "decode":
+        ch = inputs.make_decode_chain(dev, **index_kw(args))
+        iw = ch.index
+    else:
+        ch, iw = None, inputs.make_index_workload(dev, **index_kw(args))
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.zeros(sda.workspace_bytes(iw.rows, 16, 1), dtype=torch.uint8, device=dev)
+    scores = torch.empty((iw.rows, iw.n_cols), dtype=torch.float32, device=dev)
+    cur = torch.empty(iw.rows, dtype=torch.int32, device=dev) if ch else None
+    lens = torch.empty(iw.rows, dtype=torch.int32, device=dev) if ch else None
+    if ch:
+        regions = torch.empty((iw.rows, ch.topk), dtype=torch.int32, device=dev)
+        out = torch.empty_like(ch.query)
+        ks = torch.tensor([ch.k_scale], dtype=torch.float32, device=dev)
+        vs = torch.tensor([ch.v_scale], dtype=torch.float32, device=dev)
+
+    def step(iq=iw.query, iwt=iw.weights, bt=iw.block_table, seq=iw.seq_lens, q=None, pos=None, act=None,
+             s=None, marks=None):
+        s = s or stream
+        sda.sparse_decode_summary_scores(iq, iwt, iw.summaries, bt, seq, block_size=iw.block,
+                                         query_len=iw.query_len, scores=scores, current=cur, lengths=lens,
+                                         workspace=ws, stream=s)
+        if ch is None:
+            return
+        if marks:
+            marks[0].record(s)
+        sda.sparse_decode_select_regions(scores, cur, ch.topk, regions, topk_lengths=lens, stream=s)
+        if marks:
+            marks[1].record(s)
+        sda.sparse_decode_attention(ch.query if q is None else q, ch.cache, regions, bt,
+                                    ch.positions if pos is None else pos, ch.active if act is None else act,
+                                    out, scale=ch.scale, query_len=iw.query_len, splits=1, k_scale=ks,
+                                    v_scale=vs, region_tokens=8, workspace=ws, stream=s)
+
+    steps = args.steps or (200 if ch is None else 100)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    n_ev = 4 if ch else 2
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    with ClockSampler(dev.index) as clocks:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(steps):
+            ev[k][0].record(stream)
+            step(marks=ev[k][1:3] if ch else None)
+            ev[k][-1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+    region_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    flags = sda.read_errors(ws)
+    peak, peak_kind = measured_peak()
+    idx_bytes = index_traffic(iw, with_outputs=ch is not None)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    achieved = idx_bytes / (idx_ms / 1e3) / 1e9
+    value = iw.rows * steps * world / (region_ms / 1e3)
+    line = {
+        "metric": DECODE_METRIC if ch else INDEX_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": region_ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 (E4M3 operands, fp32 accumulation)",
+        "data": "synthetic", "config": index_config(kind, iw, ch.topk if ch else None),
+        "summary_gbs": idx_bytes * steps * world / (region_ms / 1e3) / 1e9 if ch is None else None,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic("index", idx_bytes, "ncu_traffic_index.txt", "sda_index.cu"),
+                     "peak_kind": peak_kind,
+                     "kernel": "sda_index_kernel", "algorithmic_bytes_per_launch": idx_bytes,
+                     "avg_launch_ms": idx_ms},
+        "gpu_launches": steps * (3 if ch else 1), "device_flags": flags, "clocks": clocks.summary(),
+    }
+    if ch:
+        sel_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        att_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
+        lens_h = lens.cpu().numpy().astype(np.int64)
+        sel_bytes = int(lens_h.sum()) * 4 + iw.rows * (12 + ch.topk * 4)
+        att_kv = iw.rows * ch.topk * 8 * inputs.ROW            # every selected region is visible
+        line["kernels"] = {
+            "sda_index_kernel": {"avg_ms": idx_ms, "gbs": achieved},
+            "sda_select_kernel": {"avg_ms": sel_ms, "gbs": sel_bytes / (sel_ms / 1e3) / 1e9},
+            "sda_split_kernel": {"avg_ms": att_ms, "selected_kv_gbs": att_kv / (att_ms / 1e3) / 1e9}}
+    if not args.no_e2e:
+        per_step = dict(iq=iw.query, iwt=iw.weights, bt=iw.block_table, seq=iw.seq_lens)
+        if ch:
+            per_step.update(q=ch.query, pos=ch.positions, act=ch.active)
+        host = {k: v.cpu().pin_memory() for k, v in per_step.items()}
+        dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+        result = out if ch else scores
+        host_out = torch.empty(result.shape, dtype=result.dtype, pin_memory=True)
+        e2e_steps = max(10, steps // 4)
+
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            step(**dev_in)
+            host_out.copy_(result, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        line["e2e"] = {"value": iw.rows * e2e_steps * world / dt, "unit": "rows/s",
+                       "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+                       "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
+                       "note": "host wall clock"}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+        rows, dt, what = cpu_index_sample(args, kind, ch or iw)
+        line["cpu_baseline"] = {"value": rows / dt, "unit": "rows/s", "cores": oracle.num_threads(),
+                                "kind": "oracle", "sample": f"{what} ({dt:.2f} s, float64 C)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_env()
@@ -387,6 +627,12 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sda.load()
+    if args.config in ("index", "decode"):
+        run_index(args, dev, world, rank, args.config)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
     if args.config == "select":
         run_select(args, dev, world, rank)
         if world > 1:

@@ -593,3 +593,46 @@ def index_host_subset(w: IndexWorkload, requests) -> IndexWorkload:
     return IndexWorkload(w.query[toks].cpu(), w.weights[toks].cpu(),
                          pages.reshape(-1, w.groups, INDEX_DIM).cpu(), torch.as_tensor(new_table),
                          w.seq_lens.cpu()[torch.as_tensor(requests)], w.block, w.query_len, w.n_cols)
+
+
+@dataclasses.dataclass
+class DecodeChain:
+    """The inputs of one DSA decode step: indexer operands, and the attention
+    operands over the same pages (FP8 K|V cache, 16 query heads per group)."""
+    index: IndexWorkload
+    cache: torch.Tensor          # [pages, G, block, 384] float8_e4m3fn
+    k_scale: float
+    v_scale: float
+    query: torch.Tensor          # [rows, 16, 192] bf16
+    positions: torch.Tensor      # [rows] int32
+    active: torch.Tensor         # [rows] bool
+    topk: int
+    scale: float = DIM ** -0.5
+
+
+def make_decode_chain(device="cpu", *, requests=512, groups=4, query_len=1,
+                      ctx=(128 * 1024, 256 * 1024), block=64, topk=1024, heads=16, seed=8,
+                      chunk_pages=1 << 14, **index_kw) -> DecodeChain:
+    """A decode step over the large workload's requests: every page of the pool
+    holds N(0,1) K|V as E4M3 with scale 8/448 (saturating beyond 8 sigma) and
+    its 8-token region summaries; the selection keeps `topk` 8-token regions
+    (1024 x 8 = 8192 tokens, the large workload's selected tokens per row)."""
+    idx = make_index_workload(device, requests=requests, groups=groups, query_len=query_len, ctx=ctx,
+                              block=block, seed=seed, **index_kw)
+    dev = torch.device(device)
+    pages = idx.summaries.shape[0] // (block // 8)
+    cache = torch.empty((pages, groups, block, ROW), dtype=torch.float8_e4m3fn, device=dev)
+    s = 8.0 / FP8_MAX
+    for p0 in range(0, pages, chunk_pages):
+        p1 = min(pages, p0 + chunk_pages)
+        x = torch.randn((p1 - p0, groups, block, ROW), generator=_gen(dev, seed * 104729 + p0), device=dev)
+        cache[p0:p1] = (x / s).clamp_(-FP8_MAX, FP8_MAX).to(torch.float8_e4m3fn)
+        del x
+    g = _gen(dev, seed + 1)
+    rows = idx.rows
+    query = torch.randn((rows, heads, DIM), generator=g, device=dev).to(torch.bfloat16)
+    seq = idx.seq_lens.to(torch.int64)
+    tok = torch.arange(idx.tokens, device=dev)
+    pos = (seq[tok // query_len] - query_len + tok % query_len).repeat_interleave(groups)
+    return DecodeChain(idx, cache, s, s, query, pos.to(torch.int32),
+                       torch.ones(rows, dtype=torch.bool, device=dev), topk)
