@@ -242,17 +242,31 @@ def run_oracle(w, hp):
                                           hp.active, gate=hp.gate, row_ids=hp.row_ids, **hp.kwargs)
 
 
+CPU_MIN_SECONDS = 10.0
+
+
+def repeat_for(fn, min_seconds=CPU_MIN_SECONDS):
+    """Run fn until at least min_seconds have passed (at least once): (runs, seconds)."""
+    runs, total = 0, 0.0
+    while runs == 0 or total < min_seconds:
+        t0 = time.perf_counter()
+        fn()
+        total += time.perf_counter() - t0
+        runs += 1
+    return runs, total
+
+
 def cpu_baseline(w, n_rows, seed=0):
-    """The float64 oracle on a bounded sample of the workload's rows."""
+    """The float64 oracle on a bounded sample of the workload's rows, repeated to
+    about 10 s of CPU work."""
     import oracle
     rng = np.random.default_rng(seed)
     rows = np.sort(rng.choice(w.rows, size=min(n_rows, w.rows), replace=False))
     hp = inputs.host_subset(w, rows)
-    t0 = time.perf_counter()
-    run_oracle(w, hp)
-    dt = time.perf_counter() - t0
-    return {"value": len(rows) / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} seeded rows of the same workload ({dt:.2f} s, float64 C, OpenMP over rows)"}
+    runs, dt = repeat_for(lambda: run_oracle(w, hp))
+    return {"value": len(rows) * runs / dt, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} seeded rows of the same workload, {runs} runs ({dt:.1f} s, float64 C, "
+                      "OpenMP over rows)"}
 
 
 def run_reference(args, world, rank):
@@ -384,11 +398,11 @@ def run_select(args, dev, world, rank):
     if rank == 0 and not args.no_cpu:
         import oracle
         n = args.cpu_rows or 256
-        t0 = time.perf_counter()
-        oracle.select_regions(sw.scores[:n].cpu(), sw.current[:n].cpu(), sw.topk, sw.lengths[:n].cpu())
-        dt = time.perf_counter() - t0
-        line["cpu_baseline"] = {"value": n / dt, "unit": "rows/s", "cores": oracle.num_threads(),
-                                "kind": "oracle", "sample": f"first {n} rows ({dt:.2f} s, full sort per row)"}
+        sc, cu, ln = sw.scores[:n].cpu(), sw.current[:n].cpu(), sw.lengths[:n].cpu()
+        runs, dt = repeat_for(lambda: oracle.select_regions(sc, cu, sw.topk, ln))
+        line["cpu_baseline"] = {"value": n * runs / dt, "unit": "rows/s", "cores": oracle.num_threads(),
+                                "kind": "oracle",
+                                "sample": f"first {n} rows, {runs} runs ({dt:.1f} s, full sort per row)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -440,24 +454,22 @@ def oracle_chain(ch, sub, cache, query, positions, active):
                                           k_scale=ch.k_scale, v_scale=ch.v_scale, cache_fp8=True)
 
 
-def cpu_index_sample(args, kind, src, k=0):
-    """One bounded oracle sample: (rows, seconds, description)."""
+def cpu_index_sample(args, kind, src, k=0, min_seconds=0.0):
+    """One bounded oracle sample, repeated for min_seconds: (rows, seconds, description)."""
     import oracle
     iw = src.index if kind == "decode" else src
     n_req = args.cpu_rows or (1 if kind == "decode" else 2)
     reqs = sorted(np.random.default_rng(2000 + k).choice(iw.seq_lens.shape[0], size=n_req, replace=False))
     if kind == "decode":
         hs = chain_host_subset(src, reqs)
-        t0 = time.perf_counter()
-        oracle_chain(src, *hs)
+        runs, dt = repeat_for(lambda: oracle_chain(src, *hs), min_seconds)
     else:
         sub = inputs.index_host_subset(iw, reqs)
-        t0 = time.perf_counter()
-        oracle.summary_scores(sub.query, sub.weights, sub.summaries, sub.block_table, sub.seq_lens,
-                              block=iw.block, n_cols=iw.n_cols, query_len=iw.query_len)
-    dt = time.perf_counter() - t0
+        runs, dt = repeat_for(lambda: oracle.summary_scores(
+            sub.query, sub.weights, sub.summaries, sub.block_table, sub.seq_lens, block=iw.block,
+            n_cols=iw.n_cols, query_len=iw.query_len), min_seconds)
     rows = n_req * iw.groups * iw.query_len
-    return rows, dt, f"{rows} rows of {n_req} seeded request(s) per sample"
+    return rows * runs, dt, f"{rows} rows of {n_req} seeded request(s), {runs} run(s)"
 
 
 def index_config(kind, iw, topk=None):
@@ -603,7 +615,7 @@ def run_index(args, dev, world, rank, kind):
                        "note": "host wall clock"}
     if rank == 0 and world == 1 and not args.no_cpu:
         import oracle
-        rows, dt, what = cpu_index_sample(args, kind, ch or iw)
+        rows, dt, what = cpu_index_sample(args, kind, ch or iw, min_seconds=CPU_MIN_SECONDS)
         line["cpu_baseline"] = {"value": rows / dt, "unit": "rows/s", "cores": oracle.num_threads(),
                                 "kind": "oracle", "sample": f"{what} ({dt:.2f} s, float64 C)"}
     if rank == 0:
