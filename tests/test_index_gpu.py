@@ -80,6 +80,8 @@ CASES = {
     "short_ql4": dict(requests=4, groups=2, query_len=4, ctx=(1, 3), block=16),
     "g4_ql4_long": dict(requests=2, groups=4, query_len=4, ctx=(30000, 40000), block=32),
     "g2_ql1_ragged": dict(requests=7, groups=2, query_len=1, ctx=(511 * 8, 513 * 8 + 7), block=64),
+    "g3_ql2": dict(requests=3, groups=3, query_len=2, ctx=(700, 6000), block=32),
+    "g6_ql1": dict(requests=3, groups=6, query_len=1, ctx=(3000, 9000), block=64),
 }
 
 
@@ -188,3 +190,49 @@ def test_decode_chain_scores_select_attention():
                                          query_len=w.query_len, region_tokens=8)
     err = np.abs(out.float().cpu().numpy() - ref).max()
     assert err <= 2e-2, err
+
+
+def test_decode_chain_full_size_sampled():
+    """The whole decode step at full size (512 requests x 4 groups, contexts
+    128K-256K, top-1024 of 8-token regions, FP8 cache) in the launch
+    configuration the benchmark times; sampled requests checked step by step."""
+    ch = inputs.make_decode_chain(DEV)
+    iw = ch.index
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    scores = torch.empty((iw.rows, iw.n_cols), device=DEV)
+    cur = torch.empty(iw.rows, dtype=torch.int32, device=DEV)
+    lens = torch.empty(iw.rows, dtype=torch.int32, device=DEV)
+    sda.sparse_decode_summary_scores(iw.query, iw.weights, iw.summaries, iw.block_table, iw.seq_lens,
+                                     block_size=iw.block, query_len=iw.query_len, scores=scores,
+                                     current=cur, lengths=lens, workspace=ws)
+    regions = sda.sparse_decode_select_regions(scores, cur, ch.topk, topk_lengths=lens)
+    out = torch.empty_like(ch.query)
+    ks = torch.tensor([ch.k_scale], device=DEV)
+    vs = torch.tensor([ch.v_scale], device=DEV)
+    sda.sparse_decode_attention(ch.query, ch.cache, regions, iw.block_table, ch.positions, ch.active, out,
+                                scale=ch.scale, query_len=iw.query_len, splits=1, k_scale=ks, v_scale=vs,
+                                region_tokens=8, workspace=ws)
+    torch.cuda.synchronize()
+    assert sda.read_errors(ws) == 0
+    reqs = [5, 300]
+    rows = [r * iw.groups + g for r in reqs for g in range(iw.groups)]
+    sub = inputs.index_host_subset(iw, reqs)
+    check((scores[rows].cpu().numpy(), cur[rows].cpu().numpy(), lens[rows].cpu().numpy()),
+          run_oracle(sub), run_oracle(sub, absolute=True)[0])
+    sel = regions[rows].cpu().numpy()
+    assert np.array_equal(sel, oracle.select_regions(scores[rows].cpu(), cur[rows].cpu(), ch.topk,
+                                                     lens[rows].cpu()))
+    assert (sel >= 0).all()                          # every row has > 1024 regions to choose from
+    # attention of the sampled rows over their own selected regions, on the requests' pages
+    table = iw.block_table.cpu().numpy()
+    used = sorted({int(p) for r in reqs for p in table[r] if p >= 0})
+    remap = np.full(int(table.max()) + 1, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    sub_table = np.where(table[reqs] >= 0, remap[np.maximum(table[reqs], 0)], -1).astype(np.int32)
+    cache = ch.cache[torch.as_tensor(used, device=DEV)].cpu()
+    ref = oracle.sparse_decode_attention(ch.query[rows].cpu(), cache, regions[rows].cpu(), sub_table,
+                                         ch.positions[rows].cpu(), ch.active[rows].cpu(), scale=ch.scale,
+                                         query_len=iw.query_len, region_tokens=8, k_scale=ch.k_scale,
+                                         v_scale=ch.v_scale, cache_fp8=True)
+    err = np.abs(out[rows].float().cpu().numpy() - ref).max()
+    assert err <= 5e-2, err
