@@ -75,6 +75,7 @@ struct Traits<false> {                     // bf16: 768 B per token; 4 stages of
     static constexpr int kBandBytes = kSlots * 128;
 };
 constexpr int kWarpsPerStage = 2;
+constexpr int kIdBatch = 8;               // region-id loads in flight per producer lane
 constexpr int kPairs = kConsumerWarps / kWarpsPerStage;
 
 constexpr int align_up(int x, int a)
@@ -465,17 +466,26 @@ __global__ void __launch_bounds__(kThreads, 2)
             n_live = pos >= 0 ? pos / P - win_base + 1 : 0;
         } else {
             // read whatever `active` says (the loads overlap), then drop inactive rows
+            // ids are loaded kIdBatch x 32 at a time so their latencies overlap
             const int32_t *reg = p.regions + static_cast<int64_t>(row) * p.reg_s0;
-            for (int j0 = 0; j0 < p.num_regions; j0 += 32) {
-                const int j = j0 + lane;
-                const int id = j < p.num_regions ? reg[j] : -1;
-                if (act && id < -1)
-                    atomicOr(p.flags, SDA_FLAG_BOUNDS);
-                const bool ok = act && id >= 0 && static_cast<int64_t>(id) * p.region_tokens <= pos;
-                const unsigned m = __ballot_sync(~0u, ok);
-                if (ok)
-                    live[n_live + __popc(m & ((1u << lane) - 1u))] = id;
-                n_live += __popc(m);
+            for (int j0 = 0; j0 < p.num_regions; j0 += 32 * kIdBatch) {
+                int ids[kIdBatch];
+#pragma unroll
+                for (int b = 0; b < kIdBatch; ++b) {
+                    const int j = j0 + 32 * b + lane;
+                    ids[b] = j < p.num_regions ? __ldg(reg + j) : -1;
+                }
+#pragma unroll
+                for (int b = 0; b < kIdBatch; ++b) {
+                    const int id = ids[b];
+                    if (act && id < -1)
+                        atomicOr(p.flags, SDA_FLAG_BOUNDS);
+                    const bool ok = act && id >= 0 && static_cast<int64_t>(id) * p.region_tokens <= pos;
+                    const unsigned m = __ballot_sync(~0u, ok);
+                    if (ok)
+                        live[n_live + __popc(m & ((1u << lane) - 1u))] = id;
+                    n_live += __popc(m);
+                }
             }
         }
         __syncwarp();
