@@ -9,7 +9,8 @@
 // (NaN lowest, ties to the lower id), and the output lists the current region
 // first, then the others in ascending id order, padded with -1.
 //
-// One CTA per row, scores compared as order-preserving 32-bit keys.
+// One CTA of 256 threads per row (3 per SM), scores compared as
+// order-preserving 32-bit keys; the row is prefetched into L2 at entry.
 //   Fast path (rows of up to 64K candidates): a low threshold is estimated
 //   from a 2048-score sample so that about 2 * topk scores pass it; one
 //   streaming pass keeps the passing (key, id) pairs in shared memory; an
@@ -26,7 +27,7 @@
 
 namespace {
 
-constexpr int kSelThreads = 512;
+constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBatch = 8;                     // loads in flight per thread (exact passes)
 constexpr int kFilterBatch = 16;                 // loads in flight per thread (filter pass)
@@ -74,6 +75,18 @@ __device__ __forceinline__ uint32_t score_key(float x)
     if ((u & 0x7FFFFFFFu) == 0u)
         u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Starts pulling bytes [p, p + n) of global memory into L2 (no data is
+// returned): one bulk prefetch of the 16-byte-aligned interior.
+__device__ __forceinline__ void prefetch_l2(const void *p, size_t n)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const uintptr_t lo = (a + 15) & ~static_cast<uintptr_t>(15);
+    const uintptr_t hi = (a + n) & ~static_cast<uintptr_t>(15);
+    if (hi > lo)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(lo), "r"(static_cast<uint32_t>(hi - lo))
+                     : "memory");
 }
 
 // Exclusive block-wide prefix sum of `v` in thread order; *total gets the
@@ -217,7 +230,7 @@ __device__ uint32_t select_global(SelShared &sh, const float *sc, int len, int c
     return prefix;
 }
 
-__global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_constant__ SelectParams p)
+__global__ void __launch_bounds__(kSelThreads, 3) sda_select_kernel(const __grid_constant__ SelectParams p)
 {
     extern __shared__ __align__(16) unsigned char sel_smem[];
     SelShared &sh = *reinterpret_cast<SelShared *>(sel_smem);
@@ -232,8 +245,12 @@ __global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_co
     const int k = p.topk - (forced ? 1 : 0);      // others to keep
     const int cand = len - (forced ? 1 : 0);      // others available
     const int base = forced ? 1 : 0;
-    if (forced && tid == 0)
-        out[0] = cur;
+    if (tid == 0) {
+        if (len > 0)
+            prefetch_l2(sc, static_cast<size_t>(len) * sizeof(float));
+        if (forced)
+            out[0] = cur;
+    }
 
     // Keep every key > thr and the first take_eq keys == thr in id order;
     // take_all keeps every candidate, k <= 0 keeps none.
@@ -258,6 +275,9 @@ __global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_co
         if (tid == 0)
             sh.counter = 0;
         __syncthreads();
+        // Each thread marks its kept scores in a bit mask; one warp scan and one
+        // shared counter update per batch place them.
+        const int excl = forced ? cur : -1;
         for (int b0 = 0; b0 < len; b0 += kSelThreads * kFilterBatch) {
             float v[kFilterBatch];
 #pragma unroll
@@ -265,19 +285,36 @@ __global__ void __launch_bounds__(kSelThreads) sda_select_kernel(const __grid_co
                 const int i = b0 + e * kSelThreads + tid;
                 v[e] = i < len ? sc[i] : 0.0f;
             }
+            uint32_t keys[kFilterBatch];
+            uint32_t keepm = 0;
 #pragma unroll
             for (int e = 0; e < kFilterBatch; ++e) {
                 const int i = b0 + e * kSelThreads + tid;
-                const uint32_t key = score_key(v[e]);
-                const bool keep = i < len && !(forced && i == cur) && key >= t_lo;
-                const unsigned m = __ballot_sync(~0u, keep);
-                uint32_t at = 0;
-                if (lane == 0 && m)
-                    at = atomicAdd(&sh.counter, static_cast<uint32_t>(__popc(m)));
-                at = __shfl_sync(~0u, at, 0) + __popc(m & ((1u << lane) - 1u));
-                if (keep && at < static_cast<uint32_t>(kBufCap)) {
-                    sh.buf_key[at] = key;
-                    sh.buf_id[at] = i;
+                keys[e] = score_key(v[e]);
+                keepm |= static_cast<uint32_t>(i < len && i != excl && keys[e] >= t_lo) << e;
+            }
+            const int cnt = __popc(keepm);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(~0u, incl, o);
+                if (lane >= o)
+                    incl += x;
+            }
+            uint32_t wbase = 0;
+            if (lane == 31 && incl)
+                wbase = atomicAdd(&sh.counter, static_cast<uint32_t>(incl));
+            uint32_t at = __shfl_sync(~0u, wbase, 31) + static_cast<uint32_t>(incl - cnt);
+            if (keepm) {
+#pragma unroll
+                for (int e = 0; e < kFilterBatch; ++e) {
+                    if ((keepm >> e) & 1u) {
+                        if (at < static_cast<uint32_t>(kBufCap)) {
+                            sh.buf_key[at] = keys[e];
+                            sh.buf_id[at] = b0 + e * kSelThreads + tid;
+                        }
+                        ++at;
+                    }
                 }
             }
         }
