@@ -575,6 +575,31 @@ def run_index(args, dev, world, rank, kind):
                      "avg_launch_ms": idx_ms},
         "gpu_launches": steps * (3 if ch else 1), "device_flags": flags, "clocks": clocks.summary(),
     }
+    # ---- the same step replayed from a CUDA graph (no host launch work per step)
+    try:
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gstream):
+            step(s=gstream)
+            gstream.synchronize()
+            with torch.cuda.graph(graph, stream=gstream):
+                step(s=gstream)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        g_ev = []
+        for _ in range(max(10, steps // 4)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            g_ev.append((a, b))
+        torch.cuda.synchronize()
+        line["graph_ms_per_step"] = statistics.median(x.elapsed_time(y) for x, y in g_ev)
+    except RuntimeError as e:                      # reported, never fatal to the bench line
+        line["graph_ms_per_step"] = None
+        line["graph_error"] = str(e)[:200]
     if ch:
         sel_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
         att_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in ev)
