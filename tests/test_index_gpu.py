@@ -236,3 +236,17 @@ def test_decode_chain_full_size_sampled():
                                          v_scale=ch.v_scale, cache_fp8=True)
     err = np.abs(out[rows].float().cpu().numpy() - ref).max()
     assert err <= 5e-2, err
+
+
+def test_padded_summary_slots():
+    """Summary slots with a padded stride (the slot's G x 256 bytes followed by 64 unused)."""
+    w = inputs.make_index_workload(DEV, requests=4, groups=2, query_len=1, ctx=(900, 5000), block=32, seed=12)
+    slots = w.summaries.shape[0]
+    big = torch.zeros((slots, w.groups * 256 + 64), dtype=torch.uint8, device=DEV)
+    big[:, :w.groups * 256] = w.summaries.view(torch.uint8).reshape(slots, -1)
+    big[:, w.groups * 256:] = 0x7F                              # NaN codes in the padding
+    padded = big[:, :w.groups * 256].view(slots, w.groups, 256)
+    assert padded.stride(0) == w.groups * 256 + 64
+    h = host(w)
+    w.summaries = padded
+    check(run_gpu(w), run_oracle(h), run_oracle(h, absolute=True)[0])
