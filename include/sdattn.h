@@ -92,9 +92,10 @@ size_t sparse_decode_workspace_bytes(int rows, int heads, int splits);
  *                K in elements 0..191 and V in 192..383 of a token's row.
  *                stride[3] == 1; any page / group / token strides whose byte
  *                sizes are multiples of 16 (and a 16-byte aligned base).
- *   regions      [rows, R] int32, stride[1] == 1.  Region ids of the row, any
- *                order; -1 marks an unused slot.  Id `id` covers the request's
- *                logical tokens [id*RT, (id+1)*RT), RT = region_tokens.
+ *   regions      [rows, R] int32, stride[1] == 1, R <= 16384 (else
+ *                SDA_ERR_UNSUPPORTED).  Region ids of the row, any order; -1
+ *                marks an unused slot.  Id `id` covers the request's logical
+ *                tokens [id*RT, (id+1)*RT), RT = region_tokens.
  *   block_table  [requests, W] int32, stride[1] == 1.  Logical block c of
  *                request q lives in page block_table[q, c].  The G*query_len
  *                consecutive rows of one request share its table row:

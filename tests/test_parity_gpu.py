@@ -152,6 +152,22 @@ def test_fp8_pages_of_48_tokens():
         check(w, out, ref, rows)
 
 
+def test_region_slots_at_the_limit():
+    """16,384 region slots per row (the most the entry point takes): every visible 8-token
+    region selected, the rest -1; one slot more is refused."""
+    w = mini("gqa", requests=2, ctx=(9000, 12000), region_tokens=8, num_regions=16384, fp8=True)
+    rows = list(range(w.rows))
+    out, flags = run(w, splits=1)
+    assert flags == 0
+    check(w, out, oracle_rows(w, rows), rows)
+    wide = torch.full((w.rows, 16385), -1, dtype=torch.int32, device=DEV)
+    wide[:, :16384] = w.regions
+    w.regions = wide
+    with pytest.raises(sda.SdaError) as e:
+        run(w, splits=1)
+    assert e.value.status == 2                        # SDA_ERR_UNSUPPORTED
+
+
 def test_many_regions_per_row():
     w = mini("gqa", requests=3, ctx=(9000, 12000), region_tokens=8, num_regions=1024, fp8=True)
     rows = list(range(w.rows))
