@@ -87,17 +87,21 @@ constexpr int align_up(int x, int a)
 // ring (1024-aligned stages for the 128-byte swizzle), mbarriers, stage
 // headers, control words, per-warp softmax statistics, gate factors, the Q
 // fragment array (16-byte vector accesses) and the row's live region list.
-template <bool FP8>
+// With PAIR (two query tokens per CTA) the headers, gate factors and Q
+// fragments come twice, one set per token.
+template <bool FP8, bool PAIR = false>
 struct Layout {
+    static constexpr int kTokens = PAIR ? 2 : 1;
     static constexpr int kStageBytes = Traits<FP8>::kBands * Traits<FP8>::kBandBytes;
     static constexpr int kRing = Traits<FP8>::kStages * kStageBytes;
     static constexpr int kBarOff = kRing;
-    static constexpr int kHdrOff = align_up(kBarOff + 16 * Traits<FP8>::kStages, 16);
-    static constexpr int kCtlOff = align_up(kHdrOff + 8 * Traits<FP8>::kStages, 16);
+    static constexpr int kHdrOff = align_up(kBarOff + 16 * Traits<FP8>::kStages, 16);   // [token][stage]
+    static constexpr int kCtlOff = align_up(kHdrOff + 8 * Traits<FP8>::kStages * kTokens, 16);
     static constexpr int kMlOff = kCtlOff + 64;
     static constexpr int kGammaOff = align_up(kMlOff + kConsumerWarps * kMaxHeads * 2 * 4, 16);
-    static constexpr int kQOff = align_up(kGammaOff + kMaxHeads * 4, 128);   // [12][32] x 16 B
-    static constexpr int kLiveOff = align_up(kQOff + 12 * 32 * 16, 16);
+    static constexpr int kQOff = align_up(kGammaOff + kTokens * kMaxHeads * 4, 128);   // [token][12][32] x 16 B
+    static constexpr int kQBytes = 12 * 32 * 16;
+    static constexpr int kLiveOff = align_up(kQOff + kTokens * kQBytes, 16);
     static_assert(kStageBytes % 1024 == 0 && Traits<FP8>::kBandBytes % 1024 == 0, "swizzle atoms");
     static_assert(Traits<FP8>::kSlots == kWarpsPerStage * Traits<FP8>::kWarpTokens, "stage split");
     static_assert(kBarOff % 8 == 0 && kHdrOff % 8 == 0 && kQOff % 16 == 0, "alignment");
@@ -395,13 +399,17 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
 // ---------------------------------------------------------------------------
 
 // FULL: a piece fills a whole stage (P = slots per stage), so the stage
-// layout is a compile-time [band][slot] one.
-template <bool FP8, bool WINDOW, bool FULL>
+// layout is a compile-time [band][slot] one.  PAIR (window mode, one split):
+// a CTA serves two consecutive query tokens of a request and group, whose
+// windows are one token apart; the producer streams their union once, each
+// warp pair computes one token over every stage.
+template <bool FP8, bool WINDOW, bool FULL, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 2)
     sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
 {
+    static_assert(!PAIR || WINDOW, "token pairs are a window-mode layout");
     using T = Traits<FP8>;
-    using L = Layout<FP8>;
+    using L = Layout<FP8, PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -413,18 +421,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *ml = reinterpret_cast<float *>(smem + L::kMlOff);
     float *gam = reinterpret_cast<float *>(smem + L::kGammaOff);
     int *live = reinterpret_cast<int *>(smem + L::kLiveOff);
-    const uint32_t qfrag = sbase + L::kQOff;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x / p.splits;
-    const int split = blockIdx.x - row * p.splits;
+    // this warp's Q fragment array (PAIR: its warp pair's token)
+    const uint32_t qfrag = sbase + L::kQOff + (PAIR && warp < kConsumerWarps ? (warp >> 1) * L::kQBytes : 0);
+    // With PAIR, CTA u serves rows (token 2k, group g) and (token 2k + 1, g),
+    // u = k * G + g (one split); `row` is the first of them.
+    const int row = PAIR ? static_cast<int>((blockIdx.x / p.groups) * 2 * p.groups + blockIdx.x % p.groups)
+                         : static_cast<int>(blockIdx.x / p.splits);
+    const int split = PAIR ? 0 : static_cast<int>(blockIdx.x - row * p.splits);
 
     if (warp == kConsumerWarps) {          // the producer warp owns the pipeline barriers
         if (lane == 0) {
             for (int s = 0; s < T::kStages; ++s) {
                 mbar_init(full_bar + 8 * s, 1);
-                mbar_init(empty_bar + 8 * s, kWarpsPerStage);
+                mbar_init(empty_bar + 8 * s, PAIR ? kConsumerWarps : kWarpsPerStage);
             }
             mbar_init_fence();
             prefetch_tmap(&tmap);
@@ -449,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Producer-only row state.
     int64_t req = 0, win_lo = 0;
     int pos = 0, P = 0, npr = 0, win_base = 0;
+    int pos_a = 0;                             // PAIR: the first token's position
+    int64_t lo_b = 0;                          // PAIR: the second token's first visible token
     if (warp == kConsumerWarps) {
         req = row / (p.groups * p.query_len);
         pos = windowed ? p.seq_lens[req] - p.query_len + (row / p.groups) % p.query_len
@@ -457,6 +471,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         npr = p.region_tokens / P;             // pieces per region (1 in window mode)
         win_lo = windowed ? max(0, pos - p.window + 1) : 0;   // first visible token
         win_base = static_cast<int>(win_lo / P);              // its piece index
+        if (PAIR) {                            // stream the union [window start of token a, pos of b]
+            pos_a = pos;
+            pos = pos_a + 1;
+            lo_b = max(0, pos - p.window + 1);
+        }
     }
 
     if (warp == kConsumerWarps) {
@@ -512,10 +531,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---- Consumers: Q A-fragments into shared memory, in fragment order
         // ([k-step][lane] x 4 words).  K-step kk of thread t covers the four
         // dims d0..d0+3 that its K loads deliver (see the QK loop below).
-        const uint16_t *q0 = p.query + static_cast<int64_t>(row) * p.q_s0;
+        const int qrow = PAIR ? row + (warp >> 1) * p.groups : row;   // PAIR: the warp pair's token
+        const uint16_t *q0 = p.query + static_cast<int64_t>(qrow) * p.q_s0;
         const int m0 = g, m1 = g + 8;
 #pragma unroll
-        for (int kk = warp; kk < 12; kk += kConsumerWarps) {
+        for (int kk = PAIR ? (warp & 1) : warp; kk < 12; kk += PAIR ? 2 : kConsumerWarps) {
             int d0;
             if constexpr (FP8)
                 d0 = 64 * (kk >> 2) + 16 * t + 4 * (kk & 3);
@@ -554,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t piece_bytes = static_cast<uint32_t>(P) * kRow * T::kElt;   // = one box
         int stage = 0, fill = 0, issued = 0;
         uint32_t phase = 0;
-        uint64_t mask = 0;
+        uint64_t mask = 0, mask_a = 0;         // PAIR: mask is the second token's, mask_a the first's
         bool aborted = false;
         // Candidate pieces c = 0, 1, ... are (live region lo + c / npr, piece
         // c % npr); the visible ones fill the stages densely, in that order.
@@ -591,9 +611,16 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (base + 32 < n_cand)
                 fetch(base + 32);
             // valid slots of the piece: [skip, nv) (skip > 0 only for a window's first piece)
-            const int nv = have ? static_cast<int>(min(static_cast<int64_t>(P), pos - t0 + 1)) : 0;
-            const int skip = have ? static_cast<int>(max(static_cast<int64_t>(0), win_lo - t0)) : 0;
-            const uint64_t pbits = (nv >= 64 ? ~0ull : ((1ull << nv) - 1ull)) & ~((1ull << skip) - 1ull);
+            // valid slots of the piece for a token seeing [lo, hi]: [lo - t0, hi - t0 + 1) within [0, P)
+            auto slot_bits = [&](int64_t lo, int64_t hi) -> uint64_t {
+                const int64_t nv = have ? min(static_cast<int64_t>(P), max(static_cast<int64_t>(0), hi - t0 + 1)) : 0;
+                const int64_t skip = have ? max(static_cast<int64_t>(0), lo - t0) : 0;
+                const uint64_t upto = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
+                const uint64_t below = skip >= 64 ? ~0ull : ((1ull << skip) - 1ull);
+                return upto & ~below;
+            };
+            const uint64_t pbits = slot_bits(PAIR ? lo_b : win_lo, pos);
+            const uint64_t pbits_a = PAIR ? slot_bits(win_lo, pos_a) : 0ull;
             const unsigned hv = __ballot_sync(~0u, have);
             const int rank = __popc(hv & ((1u << lane) - 1u));
             const int nh = __popc(hv);
@@ -615,26 +642,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (lane == 0 && cb)
                     mbar_expect_tx(fb, __popc(cb) * piece_bytes);
                 __syncwarp();
-                uint64_t mbits = 0;
+                uint64_t mbits = 0, mbits_a = 0;
                 if (copy) {
                     const int slot = fill + rank - done;
                     tma_load_5d(sbase + stage * L::kStageBytes + slot * piece_bytes, &tmap, 0, off, 0, grp,
                                 page, fb);
                     mbits = pbits << (slot * P);
+                    mbits_a = pbits_a << (slot * P);
                 }
                 const unsigned lo32 = __reduce_or_sync(~0u, static_cast<unsigned>(mbits));
                 const unsigned hi32 = __reduce_or_sync(~0u, static_cast<unsigned>(mbits >> 32));
                 mask |= (static_cast<uint64_t>(hi32) << 32) | lo32;
+                if constexpr (PAIR) {
+                    const unsigned alo = __reduce_or_sync(~0u, static_cast<unsigned>(mbits_a));
+                    const unsigned ahi = __reduce_or_sync(~0u, static_cast<unsigned>(mbits_a >> 32));
+                    mask_a |= (static_cast<uint64_t>(ahi) << 32) | alo;
+                }
                 fill += take;
                 done += take;
                 if (fill == pps) {
                     if (lane == 0) {
-                        hdr[stage] = mask;
+                        hdr[stage] = PAIR ? mask_a : mask;
+                        if (PAIR)
+                            hdr[T::kStages + stage] = mask;
                         mbar_arrive(fb);
                     }
                     ++issued;
                     fill = 0;
                     mask = 0;
+                    mask_a = 0;
                     if (++stage == T::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -644,7 +680,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (lane == 0) {
             if (fill > 0) {   // commit the last, partly filled stage (also after an abort)
-                hdr[stage] = mask;
+                hdr[stage] = PAIR ? mask_a : mask;
+                if (PAIR)
+                    hdr[T::kStages + stage] = mask;
                 mbar_arrive(full_bar + 8 * stage);
                 ++issued;
             }
@@ -673,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     // k-steps of 16 for PV.
     constexpr int NT = T::kWarpTokens / 8;
     constexpr int KS = T::kWarpTokens / 16;
-    const int pair = warp / kWarpsPerStage;
+    // PAIR: both warp pairs take every stage, pair k serving token k.
+    const int pair = PAIR ? 0 : warp / kWarpsPerStage;
+    const uint64_t *my_hdr = hdr + (PAIR ? (warp >> 1) * T::kStages : 0);
     const int slot0 = (warp % kWarpsPerStage) * T::kWarpTokens;
     constexpr uint64_t kWarpMask = (T::kWarpTokens >= 64) ? ~0ull : ((1ull << T::kWarpTokens) - 1ull);
 
@@ -699,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                              : tile_offset(slot0 + 16 * k2 + (vk & 8), piece_c, pps_c, pstride)) +
                        vsw * 128u;
 
-    for (int st = pair; st < n_st; st += kPairs) {
+    for (int st = pair; st < n_st; st += PAIR ? 1 : kPairs) {
         const int s = st % T::kStages;
         const uint32_t par = static_cast<uint32_t>(st / T::kStages) & 1u;
         const bool ok = mbar_wait(full_bar + 8 * s, par, p.wait_ns);
@@ -708,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 atomicOr(p.flags, SDA_FLAG_TIMEOUT);
             break;
         }
-        const uint32_t wm = static_cast<uint32_t>((hdr[s] >> slot0) & kWarpMask);
+        const uint32_t wm = static_cast<uint32_t>((my_hdr[s] >> slot0) & kWarpMask);
         const uint32_t stage_base = sbase + s * L::kStageBytes;
         if (wm) {
             // ---- S = Q K^T for this warp's slots: tile i, column g is slot
@@ -858,22 +898,28 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int ctid = threadIdx.x;          // 0..127 among consumers
     const int64_t tok = row / p.groups;
     const int grp = row % p.groups;
-    if (ctid < p.heads)
-        gam[ctid] = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + ctid) * p.g_s1])
-                           : 1.0f;
+    if (ctid < L::kTokens * p.heads) {     // gam[token k][head h], token k = row's token + k
+        const int k = ctid / p.heads, h = ctid - k * p.heads;
+        gam[k * kMaxHeads + h] =
+            p.gate ? gate_factor(p.gate[(tok + k) * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
+                   : 1.0f;
+    }
     consumer_bar();
 
     float fac[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int h = g + 8 * r;
+        // the warps holding this token: all four, or (PAIR) this warp's pair
+        constexpr int kMerge = PAIR ? 2 : kConsumerWarps;
+        const int w0 = PAIR ? (warp & 2) : 0;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w)
+        for (int w = w0; w < w0 + kMerge; ++w)
             M = fmaxf(M, ml[(w * kMaxHeads + h) * 2]);
         float Ls = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = w0; w < w0 + kMerge; ++w) {
             const float mw = ml[(w * kMaxHeads + h) * 2];
             if (mw != -INFINITY)
                 Ls += ml[(w * kMaxHeads + h) * 2 + 1] * fast_exp2(mw - M);
@@ -911,7 +957,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     consumer_bar();
 
     const int total = p.heads * kDim;
-    if (p.splits == 1) {
+    if constexpr (PAIR) {                  // token k's rows: warps 2k and 2k + 1
+        for (int e = ctid; e < 2 * total; e += kConsumerWarps * 32) {
+            const int k = e >= total ? 1 : 0;
+            const int r = e - k * total;
+            const int h = r / kDim, d = r - h * kDim;
+            const float v = (obuf[((2 * k) * kMaxHeads + h) * kObufStride + d] +
+                             obuf[((2 * k + 1) * kMaxHeads + h) * kObufStride + d]) *
+                            vfold * gam[k * kMaxHeads + h];
+            uint16_t *out = p.output + static_cast<int64_t>(row + k * p.groups) * p.o_s0;
+            out[static_cast<int64_t>(h) * p.o_s1 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        }
+    } else if (p.splits == 1) {
         if (!act && !p.clear_inactive)
             return;
         uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0;
@@ -1031,7 +1088,7 @@ bool dims_ok(const sda_tensor *t, int ndim)
 
 // The dynamic shared memory limit each kernel instantiation has been raised to,
 // per device.
-template <bool FP8, bool WINDOW, bool FULL>
+template <bool FP8, bool WINDOW, bool FULL, bool PAIR>
 cudaError_t ensure_smem(size_t bytes)
 {
     static std::mutex mu;
@@ -1044,32 +1101,33 @@ cudaError_t ensure_smem(size_t bytes)
     size_t &cur = raised[dev & 63];
     if (bytes <= cur)
         return cudaSuccess;
-    e = cudaFuncSetAttribute(sda_split_kernel<FP8, WINDOW, FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(sda_split_kernel<FP8, WINDOW, FULL, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(bytes));
     if (e == cudaSuccess)
         cur = bytes;
     return e;
 }
 
-template <bool FP8, bool WINDOW, bool FULL>
+template <bool FP8, bool WINDOW, bool FULL, bool PAIR = false>
 sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, cudaStream_t stream)
 {
-    const size_t smem = Layout<FP8>::bytes(num_regions);
+    const size_t smem = Layout<FP8, PAIR>::bytes(num_regions);
     if (smem > 227 * 1024)
         return SDA_ERR_UNSUPPORTED;
-    if (ensure_smem<FP8, WINDOW, FULL>(smem) != cudaSuccess)
+    if (ensure_smem<FP8, WINDOW, FULL, PAIR>(smem) != cudaSuccess)
         return SDA_ERR_CUDA;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(prm.rows) * static_cast<unsigned>(prm.splits));
+    cfg.gridDim = dim3(PAIR ? static_cast<unsigned>(prm.rows / 2)
+                            : static_cast<unsigned>(prm.rows) * static_cast<unsigned>(prm.splits));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8, WINDOW, FULL>, tmap, prm) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, sda_split_kernel<FP8, WINDOW, FULL, PAIR>, tmap, prm) != cudaSuccess)
         return SDA_ERR_CUDA;
     if (prm.splits > 1) {
         cudaLaunchConfig_t c2 = {};
@@ -1333,11 +1391,20 @@ sda_status run_call(const Call &c)
     cudaStream_t s = static_cast<cudaStream_t>(c.stream);
     const int nr = windowed ? 0 : prm.num_regions;
     const bool full = piece == stage_tokens;
+    // Window rows come in token pairs of one request (query_len even): one CTA
+    // streams the pair's union window once.
+    const bool pair = windowed && c.query_len % 2 == 0 && c.splits == 1;
     if (fp8) {
+        if (pair)
+            return full ? launch<true, true, true, true>(tmap, prm, nr, s)
+                        : launch<true, true, false, true>(tmap, prm, nr, s);
         if (windowed)
             return full ? launch<true, true, true>(tmap, prm, nr, s) : launch<true, true, false>(tmap, prm, nr, s);
         return full ? launch<true, false, true>(tmap, prm, nr, s) : launch<true, false, false>(tmap, prm, nr, s);
     }
+    if (pair)
+        return full ? launch<false, true, true, true>(tmap, prm, nr, s)
+                    : launch<false, true, false, true>(tmap, prm, nr, s);
     if (windowed)
         return full ? launch<false, true, true>(tmap, prm, nr, s) : launch<false, true, false>(tmap, prm, nr, s);
     return full ? launch<false, false, true>(tmap, prm, nr, s) : launch<false, false, false>(tmap, prm, nr, s);
