@@ -369,6 +369,10 @@ def run_select(args, dev, world, rank):
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with ClockSampler(dev.index) as clocks:
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
         for k in range(steps):
             if flush:
                 scratch.zero_()
@@ -376,6 +380,8 @@ def run_select(args, dev, world, rank):
             step()
             ev[k][1].record(stream)
         torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
     per = [a.elapsed_time(b) for a, b in ev]
     timed_ms = max_over_ranks(sum(per), dev)
     peak, peak_kind = measured_peak()
