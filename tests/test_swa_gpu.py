@@ -81,11 +81,17 @@ def test_swa_window_one_returns_v():
         assert torch.equal(out[r].view(torch.int16), v.expand(w.heads, 192).contiguous().view(torch.int16))
 
 
-def test_swa_rows_before_the_sequence_start_are_zero():
+@pytest.mark.parametrize("splits", [1, 2])       # 1: token pairs share a CTA
+def test_swa_rows_before_the_sequence_start_are_zero(splits):
     w = mini(requests=4, ctx=(900, 3000), window=64, query_len=2)
     w.seq_lens[0] = 1          # token 0 of request 0 would sit at position -1
-    out, flags = run_swa(w, splits=2)
+    w.seq_lens[1] = 2          # request 1's tokens sit at positions 0 and 1
+    ql = w.query_len
+    tok = torch.arange(w.rows // w.groups, device=w.seq_lens.device)
+    w.positions = (w.seq_lens.long()[tok // ql] - ql + tok % ql).repeat_interleave(w.groups).to(torch.int32)
+    out, flags = run_swa(w, splits=splits)
     assert flags == 0
     G = w.groups
     assert (out[:G].view(torch.int16) == 0).all()        # request 0, token 0: every group
-    assert torch.isfinite(out.float()).all()
+    rows = list(range(w.rows))
+    check(w, out, oracle_swa_rows(w, rows), rows)
