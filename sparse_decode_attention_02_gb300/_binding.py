@@ -132,13 +132,15 @@ def workspace_bytes(rows: int, heads: int, splits: int) -> int:
 _workspaces: dict = {}
 
 
-def default_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A zero-initialised per-device workspace, grown on demand.  Calls that
-    run concurrently on different streams must pass their own workspace."""
-    key = torch.device(device)
+def default_workspace(device: torch.device, nbytes: int, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """A zero-initialised workspace per (device, stream), grown on demand: calls
+    on one stream are ordered, so they can share it; another stream gets its own."""
+    device = torch.device(device)
+    handle = stream.cuda_stream if stream is not None else torch.cuda.current_stream(device).cuda_stream
+    key = (device, handle)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 1 << 12), dtype=torch.uint8, device=key)
+        ws = torch.zeros(max(nbytes, 1 << 12), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 
@@ -168,7 +170,7 @@ def sparse_decode_attention(query, cache, regions, block_table, positions, activ
         splits = lib.sparse_decode_splits(rows)
     need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
     if workspace is None:
-        workspace = default_workspace(query.device, need)
+        workspace = default_workspace(query.device, need, stream)
     ks, _keep_k = _scale_ptr(k_scale, query.device)
     vs, _keep_v = _scale_ptr(v_scale, query.device)
     descs = [describe(x) for x in (query, cache, regions, block_table, positions, active, output)]
@@ -200,7 +202,7 @@ def sparse_decode_swa_attention(query, cache, block_table, seq_lens, output, *, 
         splits = lib.sparse_decode_swa_splits(rows, int(window))
     need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
     if workspace is None:
-        workspace = default_workspace(query.device, need)
+        workspace = default_workspace(query.device, need, stream)
     ks, _keep_k = _scale_ptr(k_scale, query.device)
     vs, _keep_v = _scale_ptr(v_scale, query.device)
     descs = [describe(x) for x in (query, cache, block_table, seq_lens, output)]

@@ -338,3 +338,24 @@ def test_deterministic_and_graph_capturable():
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
     assert sda.read_errors(ws) == 0
+
+
+def test_default_workspaces_are_per_stream():
+    """Split calls on two streams at once, without explicit workspaces: each stream's
+    default workspace is its own, so the partials do not race."""
+    w = mini("gqa", requests=8, ctx=(4000, 9000))
+    rows = list(range(w.rows))
+    ref = oracle_rows(w, rows)
+    ks, vs = scales(w)
+    streams = [torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)]
+    outs = [torch.full_like(w.query, float("nan")) for _ in streams]
+    torch.cuda.synchronize()
+    for _ in range(20):
+        for s, o in zip(streams, outs):
+            with torch.cuda.stream(s):
+                sda.sparse_decode_attention(w.query, w.cache, w.regions, w.block_table, w.positions, w.active, o,
+                                            scale=w.scale, splits=4, k_scale=ks, v_scale=vs, gate=w.gate,
+                                            region_tokens=w.region_tokens, stream=s)
+    torch.cuda.synchronize()
+    for o in outs:
+        check(w, o, ref, rows)
