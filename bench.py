@@ -616,6 +616,12 @@ def run_index(args, dev, world, rank, kind):
             "sda_index_kernel": {"avg_ms": idx_ms, "gbs": achieved},
             "sda_select_kernel": {"avg_ms": sel_ms, "gbs": sel_bytes / (sel_ms / 1e3) / 1e9},
             "sda_split_kernel": {"avg_ms": att_ms, "selected_kv_gbs": att_kv / (att_ms / 1e3) / 1e9}}
+        # the whole step: every kernel's algorithmic bytes over the step's time
+        att_bytes = att_kv + iw.rows * (2 * 16 * inputs.DIM * 2 + ch.topk * 4)
+        step_bytes = idx_bytes + sel_bytes + att_bytes
+        line["step_algorithmic_bytes"] = step_bytes
+        line["step_gbs"] = step_bytes * steps * world / (region_ms / 1e3) / 1e9 / world
+        line["step_frac_of_peak"] = line["step_gbs"] / peak
     if not args.no_e2e:
         per_step = dict(iq=iw.query, iwt=iw.weights, bt=iw.block_table, seq=iw.seq_lens)
         if ch:
