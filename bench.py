@@ -131,11 +131,14 @@ def unique_kv_bytes(w) -> int:
             else:
                 ids = {int(i) for r in rows for i in reg[r] if i >= 0 and i * RT <= pos[r]}
                 total += sum(min(RT, pmax - i * RT + 1) for i in ids)
-    return total * 384 * elt
+    return int(total) * 384 * elt
 
 
 def traffic(w, splits):
-    """(selected K|V bytes, algorithmic bytes) per call."""
+    """(selected K|V bytes, algorithmic bytes) per call.  The sparse path's
+    algorithmic K|V is each row's visible selected tokens; the window path's is
+    the distinct tokens of each (request, group), whose query tokens' windows
+    overlap and are read once."""
     elt = 1 if w.fp8 else 2
     vis = visible_tokens(w)
     kv = int(vis.sum()) * 384 * elt
@@ -144,7 +147,8 @@ def traffic(w, splits):
     per_row = H * 192 * 2 * 2 + R * 4 + 8 + (H * 2 if w.gate is not None else 0)
     table = int(np.ceil(vis / max(1, w.block)).sum()) * 4
     ws = act * splits * H * (192 + 1) * 4 * 2 if splits > 1 else 0
-    return kv, kv + act * per_row + table + ws
+    kv_alg = unique_kv_bytes(w) if w.window else kv
+    return kv, kv_alg + act * per_row + table + ws
 
 
 class ClockSampler:
