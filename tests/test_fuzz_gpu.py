@@ -1,5 +1,5 @@
-"""Seeded random shapes through the sparse and window paths, every row against
-the oracle.
+"""Seeded random shapes through every kernel, against the oracle: the sparse and
+window paths row by row, the indexer score by score, the selection id by id.
 
 Each case draws KV groups, heads, page size, region size, region count,
 query_len, cache dtype, gate, inactive rows, -1 padding and the split count
@@ -74,3 +74,61 @@ def test_random_window_shapes(seed):
     out, flags = run_swa(w, splits=splits)
     assert flags == 0
     check(w, out, oracle_swa_rows(w, rows), rows)
+
+
+def index_case(seed):
+    rng = np.random.default_rng(3000 + seed)
+    block = int(rng.choice([8, 16, 32, 64, 128]))
+    lo = int(rng.integers(1, 3000))
+    kw = dict(requests=int(rng.integers(1, 6)), groups=int(rng.integers(1, 9)),
+              query_len=int(rng.integers(1, 5)), ctx=(lo, lo + int(rng.integers(0, 9000))), block=block,
+              seed=seed)
+    if rng.integers(0, 3) == 0:
+        kw["n_cols"] = int(rng.integers(0, 600))
+    return kw
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_indexer_shapes(seed):
+    import torch
+    import oracle
+    w = inputs.make_index_workload(DEV, **index_case(seed))
+    scores = torch.full((w.rows, w.n_cols), float("nan"), device=DEV)
+    cur = torch.full((w.rows,), -7, dtype=torch.int32, device=DEV)
+    lens = torch.full((w.rows,), -7, dtype=torch.int32, device=DEV)
+    import sparse_decode_attention_02_gb300 as sda
+    sda.sparse_decode_summary_scores(w.query, w.weights, w.summaries, w.block_table, w.seq_lens,
+                                     block_size=w.block, query_len=w.query_len, scores=scores,
+                                     current=cur, lengths=lens)
+    torch.cuda.synchronize()
+    q, m = w.query.cpu().view(torch.uint8), w.summaries.cpu().view(torch.uint8)
+    args = (w.block_table.cpu(), w.seq_lens.cpu())
+    kw = dict(block=w.block, n_cols=w.n_cols, query_len=w.query_len)
+    rs, rc, rl = oracle.summary_scores(q, w.weights.cpu(), m, *args, **kw)
+    scale, _, _ = oracle.summary_scores(q & 0x7F, w.weights.cpu().abs(), m & 0x7F, *args, **kw)
+    gs = scores.cpu().numpy()
+    assert np.array_equal(cur.cpu().numpy(), rc) and np.array_equal(lens.cpu().numpy(), rl)
+    assert np.array_equal(np.isneginf(gs), np.isneginf(rs)) and not np.isnan(gs).any()
+    fin = np.isfinite(rs)
+    assert (np.abs(gs[fin] - rs[fin]) <= 4e-5 * scale[fin] + 1e-6).all()
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_selection_inputs(seed):
+    import torch
+    import oracle
+    import sparse_decode_attention_02_gb300 as sda
+    rng = np.random.default_rng(4000 + seed)
+    rows, n = int(rng.integers(1, 40)), int(rng.integers(1, 40000))
+    topk = int(rng.integers(1, min(5000, 2 * n + 2)))
+    sc = rng.standard_normal((rows, n)).astype(np.float32)
+    if rng.integers(0, 2):                                        # heavy ties
+        sc = np.round(sc * 2) / 2
+    sc[rng.random((rows, n)) < 0.01] = np.nan
+    sc[rng.random((rows, n)) < 0.01] = -0.0
+    lens = rng.integers(0, n + 1, size=rows).astype(np.int32)
+    cur = np.array([int(rng.integers(-1, max(1, l + 1))) for l in lens], dtype=np.int32)
+    t = lambda a: torch.as_tensor(a, device=DEV)
+    got = sda.sparse_decode_select_regions(t(sc), t(cur), topk, topk_lengths=t(lens))
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), oracle.select_regions(sc, cur, topk, lens))
