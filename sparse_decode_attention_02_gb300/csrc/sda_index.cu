@@ -131,10 +131,10 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int seg)
 }
 
 // QL = tokens per request, GB = groups per CTA (4, 2 or 1, dividing G; the
-// 4 / GB warps of a group split the CTA's regions).  Each lane keeps, per token and 32-dim chunk kc,
-// the query words w0 = bytes [32kc + 4t, +4) and w1 = bytes [32kc + 16 + 4t,
-// +4) of head `gid` (lane = 4 gid + t).  For QL <= 2 they are held already
-// converted to fp16 pairs.
+// 4 / GB warps of a group split the CTA's regions).  Each lane keeps, per
+// token and 32-dim chunk kc, the query words w0 = bytes [32kc + 4t, +4) and
+// w1 = bytes [32kc + 16 + 4t, +4) of head `gid` (lane = 4 gid + t).  For
+// QL <= 2 they are held already converted to fp16 pairs.
 template <int QL, int GB>
 __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexParams p)
 {

@@ -8,16 +8,22 @@
 // Design (one CTA per (row, split) unit; 5 warps):
 //   * warp 4 (producer) compacts the row's live regions, splits them into a
 //     contiguous chunk per split, resolves each region's pages through
-//     block_table and streams "pieces" (runs of P = min(RT, B, 64) tokens of
-//     one page) into a ring of 64-token stages with TMA tensor copies
-//     (128-byte swizzled column bands of the [pages, G, B, 384] cache);
-//   * warps 0-3 (consumers) each own 16 token slots of a stage: QK^T for the
-//     16-head x 192 query tile with mma.sync m16n8k16 (heads are the M
-//     dimension), causal/validity masking, online softmax in fp32, PV with
-//     mma.sync; FP8 bytes are converted to fp16 in registers;
-//   * the epilogue merges the four warps' (max, sum, O) through shared memory
-//     and either writes the gated bf16 output (one split) or the split's fp32
+//     block_table (one lane per piece, the next batch's table entries loading
+//     meanwhile) and streams "pieces" (runs of P = min(RT, B, stage) tokens of
+//     one page) into a 4-stage ring: the lanes holding a stage's pieces issue
+//     one 5-D TMA box each (128-byte band chunks x P tokens x all bands of the
+//     [pages, G, B, 384] cache, 128-byte swizzle);
+//   * warps 0-3 (consumers) work in two pairs that take alternate stages, each
+//     warp owning half of a stage's slots: QK^T for the 16-head x 192 query
+//     tile with mma.sync m16n8k16 (heads are the M dimension), causal/validity
+//     masking, online softmax in fp32, PV with mma.sync; FP8 bytes are
+//     converted to fp16 in registers;
+//   * the epilogue merges the warps' (max, sum, O) through shared memory and
+//     either writes the gated bf16 output (one split) or the split's fp32
 //     partial output and log-sum-exp for the combine kernel.
+// Window mode walks the pieces of [pos - window + 1, pos] instead of regions;
+// with token pairs one CTA serves two query tokens of a request (their
+// overlapping windows streamed once, one warp pair per token).
 // Every mbarrier wait is bounded; a wait that runs out raises a flag in the
 // workspace header and the CTA winds down after its copies have landed.
 #include <cuda.h>
