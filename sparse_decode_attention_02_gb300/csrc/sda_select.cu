@@ -9,11 +9,12 @@
 // (NaN lowest, ties to the lower id), and the output lists the current region
 // first, then the others in ascending id order, padded with -1.
 //
-// One CTA of 256 threads per row (3 per SM), scores compared as
+// One CTA of 256 threads per row (4 per SM), scores compared as
 // order-preserving 32-bit keys; the row is prefetched into L2 at entry.
 //   Fast path (rows of up to 64K candidates): a low threshold is estimated
 //   from a 2048-score sample so that about 2 * topk scores pass it; one
-//   streaming pass keeps the passing (key, id) pairs in shared memory; an
+//   streaming pass (a plain float comparison against the threshold's
+//   smallest passing value) keeps the passing (key, id) pairs in shared memory; an
 //   exact radix select on that buffer gives the last kept key; bitmaps over
 //   the ids give the lowest-id ties and the ascending output.
 //   Fallback (buffer overflow or underflow, longer rows): an exact 4-pass
@@ -31,8 +32,10 @@ constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBatch = 8;                     // loads in flight per thread (exact passes)
 constexpr int kFilterBatch = 16;                 // loads in flight per thread (filter pass)
+constexpr int kFilterStep = kSelThreads * kFilterBatch;
 constexpr int kSample = 2048;                    // scores sampled for the filter threshold
-constexpr int kBufCap = 4096;                    // filtered (key, id) pairs held in shared memory
+constexpr int kBufCap = 4080;                    // filtered (key, id) pairs held in shared memory
+                                                 // (57,260 bytes in all: 4 CTAs per SM)
 constexpr int kFastMaxLen = 65536;               // longest row the bitmaps cover
 constexpr int kBitWords = kFastMaxLen / 32;
 
@@ -49,8 +52,7 @@ struct SelectParams {
 };
 
 struct SelShared {
-    uint32_t whist[kSelWarps][256];              // per-warp histograms
-    uint32_t hist[256];
+    uint32_t whist[kSelWarps][256];              // per-warp histograms; row 0 then holds the sums
     uint32_t cnt[kSelWarps];
     uint32_t found[2];                           // digit, keys above it
     uint32_t counter;
@@ -64,6 +66,8 @@ struct SelShared {
     uint32_t buf_key[kBufCap];
     int32_t buf_id[kBufCap];
 };
+// 4 CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
+static_assert(sizeof(SelShared) <= 4 * 1024 * 14, "selection shared memory above 4 CTAs per SM");
 
 // Order-preserving key: a larger score gives a larger key; NaN is the
 // smallest key and -0 equals +0.
@@ -75,6 +79,19 @@ __device__ __forceinline__ uint32_t score_key(float x)
     if ((u & 0x7FFFFFFFu) == 0u)
         u = 0u;
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The smallest float whose key is at least t > 0: a non-NaN x has
+// score_key(x) >= t exactly when x >= this value (NaN, which fails every
+// ordered comparison, when no float reaches t; -inf when every float does).
+__device__ __forceinline__ float key_floor_value(uint32_t t)
+{
+    if (t & 0x80000000u) {                               // +0 and the positive floats
+        const uint32_t u = t & 0x7FFFFFFFu;
+        return __uint_as_float(u > 0x7F800000u ? 0x7FC00000u : u);
+    }
+    const uint32_t u = ~t;                               // the negative floats
+    return (u & 0x7FFFFFFFu) > 0x7F800000u ? __uint_as_float(0xFF800000u) : __uint_as_float(u);
 }
 
 // Starts pulling bytes [p, p + n) of global memory into L2 (no data is
@@ -122,8 +139,9 @@ __device__ __forceinline__ void zero_whist(SelShared &sh)
         (&sh.whist[0][0])[i] = 0;
 }
 
-// Sums the per-warp histograms and finds the digit holding the key of
-// descending rank `remaining`: sh.found = {digit, keys in higher digits}.
+// Sums the per-warp histograms (into whist[0]: each bin is summed by one
+// thread) and finds the digit holding the key of descending rank
+// `remaining`: sh.found = {digit, keys in higher digits}.
 __device__ __forceinline__ void find_digit(SelShared &sh, int remaining)
 {
     const int tid = threadIdx.x;
@@ -133,14 +151,14 @@ __device__ __forceinline__ void find_digit(SelShared &sh, int remaining)
 #pragma unroll
         for (int w = 0; w < kSelWarps; ++w)
             sum += sh.whist[w][b];
-        sh.hist[b] = sum;
+        sh.whist[0][b] = sum;
     }
     __syncthreads();
     if (tid < 32) {
         uint32_t c[8], sum = 0;   // lane l: bins 255 - 8l - j, j = 0..7 (descending)
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            c[j] = sh.hist[255 - 8 * tid - j];
+            c[j] = sh.whist[0][255 - 8 * tid - j];
             sum += c[j];
         }
         uint32_t incl = sum;
@@ -230,7 +248,7 @@ __device__ uint32_t select_global(SelShared &sh, const float *sc, int len, int c
     return prefix;
 }
 
-__global__ void __launch_bounds__(kSelThreads, 3) sda_select_kernel(const __grid_constant__ SelectParams p)
+__global__ void __launch_bounds__(kSelThreads, 4) sda_select_kernel(const __grid_constant__ SelectParams p)
 {
     extern __shared__ __align__(16) unsigned char sel_smem[];
     SelShared &sh = *reinterpret_cast<SelShared *>(sel_smem);
@@ -276,22 +294,36 @@ __global__ void __launch_bounds__(kSelThreads, 3) sda_select_kernel(const __grid
             sh.counter = 0;
         __syncthreads();
         // Each thread marks its kept scores in a bit mask; one warp scan and one
-        // shared counter update per batch place them.
+        // shared counter update per batch place them.  With t_lo > 0 the test
+        // key >= t_lo is the float comparison x >= key_floor_value(t_lo), so a
+        // key is formed only for a kept score; batches wholly inside the row and
+        // clear of the current region skip the per-score id checks.
         const int excl = forced ? cur : -1;
-        for (int b0 = 0; b0 < len; b0 += kSelThreads * kFilterBatch) {
+        const bool keep_all = t_lo == 0u;
+        const float x_lo = keep_all ? 0.0f : key_floor_value(t_lo);
+        for (int b0 = 0; b0 < len; b0 += kFilterStep) {
+            const bool plain = !keep_all && b0 + kFilterStep <= len && (excl < b0 || excl >= b0 + kFilterStep);
             float v[kFilterBatch];
-#pragma unroll
-            for (int e = 0; e < kFilterBatch; ++e) {
-                const int i = b0 + e * kSelThreads + tid;
-                v[e] = i < len ? sc[i] : 0.0f;
-            }
-            uint32_t keys[kFilterBatch];
             uint32_t keepm = 0;
+            if (plain) {
+                const float *src = sc + b0 + tid;
 #pragma unroll
-            for (int e = 0; e < kFilterBatch; ++e) {
-                const int i = b0 + e * kSelThreads + tid;
-                keys[e] = score_key(v[e]);
-                keepm |= static_cast<uint32_t>(i < len && i != excl && keys[e] >= t_lo) << e;
+                for (int e = 0; e < kFilterBatch; ++e)
+                    v[e] = src[e * kSelThreads];
+#pragma unroll
+                for (int e = 0; e < kFilterBatch; ++e)
+                    keepm |= static_cast<uint32_t>(v[e] >= x_lo) << e;
+            } else {
+#pragma unroll
+                for (int e = 0; e < kFilterBatch; ++e) {
+                    const int i = b0 + e * kSelThreads + tid;
+                    v[e] = i < len ? sc[i] : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < kFilterBatch; ++e) {
+                    const int i = b0 + e * kSelThreads + tid;
+                    keepm |= static_cast<uint32_t>(i < len && i != excl && (keep_all || v[e] >= x_lo)) << e;
+                }
             }
             const int cnt = __popc(keepm);
             int incl = cnt;
@@ -310,7 +342,7 @@ __global__ void __launch_bounds__(kSelThreads, 3) sda_select_kernel(const __grid
                 for (int e = 0; e < kFilterBatch; ++e) {
                     if ((keepm >> e) & 1u) {
                         if (at < static_cast<uint32_t>(kBufCap)) {
-                            sh.buf_key[at] = keys[e];
+                            sh.buf_key[at] = score_key(v[e]);
                             sh.buf_id[at] = b0 + e * kSelThreads + tid;
                         }
                         ++at;
@@ -443,7 +475,7 @@ cudaError_t ensure_select_smem()
         return cudaSuccess;
     e = cudaFuncSetAttribute(sda_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(sizeof(SelShared)));
-    if (e == cudaSuccess)   // all of the unified L1/shared storage as shared: 3 CTAs per SM fit
+    if (e == cudaSuccess)   // all of the unified L1/shared storage as shared: 4 CTAs per SM fit
         e = cudaFuncSetAttribute(sda_select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev >= 0 && dev < 256)
@@ -471,7 +503,7 @@ extern "C" sda_status sparse_decode_select_regions(const sda_tensor *scores, con
     if (has_len && (!is_dims(topk_lengths, 1) || topk_lengths->dtype != SDA_DTYPE_INT32 ||
                     topk_lengths->shape[0] != rows))
         return SDA_ERR_INVALID;
-    if (rows > INT32_MAX || n_cols > INT32_MAX - kSelThreads * kFilterBatch)
+    if (rows > INT32_MAX || n_cols > INT32_MAX - kFilterStep)
         return SDA_ERR_UNSUPPORTED;
     if (rows == 0)
         return SDA_OK;

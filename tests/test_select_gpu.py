@@ -78,3 +78,35 @@ def test_select_then_sparse_decode():
     assert flags == 0
     rows = list(range(w.rows))
     check(w, out, oracle_rows(w, rows), rows)
+
+
+# Bit patterns at every boundary of the float order the selection follows: denormals of both
+# signs, both zeros, the infinities, NaN (both signs) and the largest finite values.
+SPECIAL_BITS = [0x00000001, 0x00000002, 0x0000FFFF, 0x00010000, 0x007FFFFF, 0x00800000,
+                0x80000001, 0x80000002, 0x8000FFFF, 0x80010000, 0x807FFFFF, 0x80800000,
+                0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000,
+                0x7F7FFFFF, 0xFF7FFFFF, 0x3F800000, 0xBF800000]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_select_special_floats(seed):
+    """Rows longer than the shared-memory buffer, so the threshold comes from a sample, built
+    from the special values above (some rows also from random denormal patterns of both signs);
+    heavy ties on every value, so the lowest-id rule decides many slots."""
+    rng = np.random.default_rng(900 + seed)
+    rows, n = 12, int(rng.integers(4500, 30000))
+    special = np.array(SPECIAL_BITS, dtype=np.uint32)
+    bits = rng.choice(special, size=(rows, n), p=rng.dirichlet(np.full(len(special), 0.4)))
+    denorm = rng.integers(1, 1 << 23, size=(rows, n), dtype=np.uint32) | \
+        (rng.integers(0, 2, size=(rows, n), dtype=np.uint32) << 31)
+    mix = (np.arange(rows) % 3 == 0)[:, None] & (rng.random((rows, n)) < 0.6)
+    bits = np.where(mix, denorm, bits)
+    sc = bits.view(np.float32)
+    lens = rng.integers(n // 2, n + 1, size=rows).astype(np.int32)
+    lens[0] = n
+    cur = np.array([int(rng.integers(-1, l)) for l in lens], dtype=np.int32)
+    t = lambda a: torch.as_tensor(a, device=DEV)
+    for topk in (1, 97, 1024, 3000):
+        got = sda.sparse_decode_select_regions(t(sc), t(cur), topk, topk_lengths=t(lens))
+        torch.cuda.synchronize()
+        assert np.array_equal(got.cpu().numpy(), oracle.select_regions(sc, cur, topk, lens)), topk
