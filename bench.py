@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--splits", type=int, default=None, help="force a split count")
     ap.add_argument("--requests", type=int, default=None, help="shrink the batch (profiling)")
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="context range override (profiling)")
+    ap.add_argument("--query-len", type=int, default=None,
+                    help="tokens per request for the index and decode configs (speculative decode)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=None)
@@ -151,60 +153,111 @@ def traffic(w, splits):
     return kv, kv_alg + act * per_row + table + ws
 
 
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# NVML clock-event reason bits (nvml.h) that bear on a timing
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index):
-        self.index = index
+
+def nvml_reasons(bits: int) -> list:
+    return sorted(name for bit, name in NVML_REASONS.items() if bits & bit)
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons during a timed region: read-only NVML
+    queries every 10 ms from a host thread (the GPU matched by its UUID), else
+    nvidia-smi every 200 ms."""
+    PERIOD_S = 0.01
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev):
+        self.dev = dev
+        self.samples = []            # (sm MHz, max sm MHz, reasons)
+        self.source = None
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.stop = threading.Event()
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            handle = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                raise OSError("no NVML device with this GPU's UUID")
+            reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            if reasons is None:
+                reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError, RuntimeError):
+            lib.nvmlShutdown()
+            raise
+        return lib, handle, reasons
+
+    def _poll_nvml(self, lib, handle, reasons):
+        import ctypes
+        clk, mx, bits = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while True:
+            if (lib.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0           # NVML_CLOCK_SM
+                    and lib.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0
+                    and reasons(handle, ctypes.byref(bits)) == 0):
+                self.samples.append((float(clk.value), float(mx.value), nvml_reasons(bits.value)))
+            if self.stop.wait(self.PERIOD_S):
+                break
+        lib.nvmlShutdown()
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            self.samples.append((sm, mx, [n for n, v in zip(names, parts[5:9]) if v.lower() == "active"]))
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            args = self._open_nvml()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll_nvml, args=args, daemon=True)
+        except (OSError, AttributeError, RuntimeError):
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.dev.index}", f"--query-gpu={self.SMI_FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                self.thread = threading.Thread(target=self._read_smi, daemon=True)
+            except OSError:
+                return self
+        self.thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
-
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        got = list(self.samples)
+        if not got:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        return {"sm_mhz": statistics.median(s[0] for s in got), "sm_max_mhz": max(s[1] for s in got),
+                "reasons": sorted({r for s in got for r in s[2]}), "samples": len(got), "source": self.source}
 
 
 def measured_peak():
@@ -372,7 +425,7 @@ def run_select(args, dev, world, rank):
         step()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
@@ -502,6 +555,8 @@ def index_kw(args) -> dict:
         kw["requests"] = args.requests
     if args.ctx:
         kw["ctx"] = tuple(args.ctx)
+    if args.query_len:
+        kw["query_len"] = args.query_len
     return kw
 
 
@@ -549,7 +604,7 @@ def run_index(args, dev, world, rank, kind):
     torch.cuda.synchronize()
     n_ev = 4 if ch else 2
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         if world > 1:
             import torch.distributed as dist
             dist.barrier()
@@ -731,7 +786,7 @@ def main():
 
     # ---- timed region: exactly `steps` calls
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    with ClockSampler(dev.index) as clocks:
+    with ClockSampler(dev) as clocks:
         barrier()
         torch.cuda.synchronize()
         t_start = torch.cuda.Event(enable_timing=True)

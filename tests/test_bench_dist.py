@@ -73,3 +73,22 @@ def test_reference_arm_index_config_under_torchrun():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["requests"] == 4
+
+
+def test_clock_sampler_reasons_and_summary():
+    """NVML reason bits map to the names the timing rules use; the summary takes the median SM
+    clock, the highest maximum and the union of reasons; no sampler source gives 'unsampled'."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.nvml_reasons(0) == []
+    assert bench.nvml_reasons(0x1 | 0x4) == ["sw_power_cap"]                      # idle bit ignored
+    assert bench.nvml_reasons(0x8 | 0x20 | 0x40) == ["hw_slowdown", "hw_thermal_slowdown",
+                                                     "sw_thermal_slowdown"]
+    c = bench.ClockSampler(torch.device("cpu"))
+    c.samples = [(2070.0, 2070.0, []), (1980.0, 2070.0, ["sw_power_cap"]), (2070.0, 2070.0, [])]
+    assert c.summary()["sm_mhz"] == 2070.0 and c.summary()["reasons"] == ["sw_power_cap"]
+    assert c.summary()["samples"] == 3 and c.summary()["sm_max_mhz"] == 2070.0
+    c = bench.ClockSampler(torch.device("cpu"))
+    c.samples = []
+    assert c.summary()["reasons"] == ["unsampled"]
