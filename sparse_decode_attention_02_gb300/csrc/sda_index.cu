@@ -17,10 +17,10 @@
 // up to 4 KV groups, one warp per group (the groups' summaries of a slot are
 // adjacent, so the CTA reads them as one run); with fewer groups per block the
 // spare warps split the chunk.  Each warp streams 1024 regions of its group as
-// 16-region tiles.  A tile (16 x 256 FP8
-// bytes, 4 KB) is copied with 16-byte cp.async into a 4-stage ring of the
-// warp's own shared memory, XOR-swizzled per row so that ldmatrix reads are
-// conflict-free.  The product is an MMA with the regions as M (16) and the 8
+// 16-region tiles.  A tile (16 x 256 FP8 bytes, 4 KB) is copied with 16-byte
+// cp.async into a 3- or 4-stage ring of the warp's own shared memory (see
+// ring_tiles), XOR-swizzled per row so that ldmatrix reads are conflict-free.
+// The product is an MMA with the regions as M (16) and the 8
 // heads of one token as N: ldmatrix gives each lane 4 contiguous summary
 // bytes per row, which serve both k16 steps of mma.sync m16n8k16 once the
 // same byte-to-k permutation is applied to the query words (every k is still
@@ -46,12 +46,19 @@ constexpr int kIdxWarps = 4;
 constexpr int kIdxThreads = kIdxWarps * 32;
 constexpr int kTile = 16;             // regions per tile (the MMA's M)
 constexpr int kTilesPerWarp = 64;
-constexpr int kStages = 4;            // tiles in a warp's ring
 constexpr int kWarpRegions = kTilesPerWarp * kTile;   // regions one warp streams
 constexpr int kTileBytes = kTile * kIdxDim;
-constexpr int kSmemBytes = kIdxWarps * kStages * kTileBytes;
 constexpr int kMaxQueryLen = 4;
-static_assert(kStages * kTile <= 64, "the ring's row masks are packed into one 64-bit word");
+
+// Tiles in a warp's ring and CTAs per SM, by tokens per request, as measured
+// on 512 requests of 128K-256K tokens: a 3-tile ring (48 KB per CTA) at 4 CTAs
+// per SM, except for 3 tokens, which ran 18 % slower that way than with a
+// 4-tile ring (64 KB per CTA) at 3 CTAs per SM.
+__host__ __device__ constexpr int ring_tiles(int ql) { return ql == 3 ? 4 : 3; }
+__host__ __device__ constexpr int ctas_per_sm(int ql) { return ql == 3 ? 3 : 4; }
+__host__ __device__ constexpr int index_smem_bytes(int ql) { return kIdxWarps * ring_tiles(ql) * kTileBytes; }
+static_assert(ring_tiles(3) * kTile <= 64 && ring_tiles(1) * kTile <= 64,
+              "the ring's row masks are packed into one 64-bit word");
 
 struct IndexParams {
     const uint8_t *query;     // [tokens, G, 8, 256]
@@ -136,9 +143,10 @@ __device__ __forceinline__ uint32_t tile_offset(int row, int seg)
 // w1 = bytes [32kc + 16 + 4t, +4) of head `gid` (lane = 4 gid + t).  For
 // QL <= 2 they are held already converted to fp16 pairs.
 template <int QL, int GB>
-__global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexParams p)
+__global__ void __launch_bounds__(kIdxThreads, ctas_per_sm(QL)) sda_index_kernel(const IndexParams p)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int kStages = ring_tiles(QL);
     constexpr bool kPreconv = QL <= 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, t4 = lane & 3;
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(kIdxThreads, 3) sda_index_kernel(const IndexPa
     }
 }
 
-cudaError_t ensure_index_smem(const void *kernel, int slot)
+cudaError_t ensure_index_smem(const void *kernel, int slot, int smem_bytes)
 {
     static std::mutex mu;
     static bool raised[kMaxQueryLen * 3][256] = {};
@@ -351,8 +359,8 @@ cudaError_t ensure_index_smem(const void *kernel, int slot)
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < 256 && raised[slot][dev])
         return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)   // three 64 KB CTAs per SM
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess)   // all of the unified L1/shared storage as shared: ctas_per_sm CTAs fit
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && dev >= 0 && dev < 256)
@@ -479,12 +487,12 @@ extern "C" sda_status sparse_decode_summary_scores(
 #undef SDA_INDEX_KERNELS
     const int gb_slot = gblock == 4 ? 2 : gblock - 1;
     const void *kernel = kernels[query_len - 1][gb_slot];
-    if (ensure_index_smem(kernel, (query_len - 1) * 3 + gb_slot) != cudaSuccess)
+    if (ensure_index_smem(kernel, (query_len - 1) * 3 + gb_slot, index_smem_bytes(query_len)) != cudaSuccess)
         return SDA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(chunks * (groups / gblock) * reqs));
     cfg.blockDim = dim3(kIdxThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = index_smem_bytes(query_len);
     cfg.stream = static_cast<cudaStream_t>(stream);
     void *args[] = {&prm};
     return cudaLaunchKernelExC(&cfg, kernel, args) == cudaSuccess ? SDA_OK : SDA_ERR_CUDA;
