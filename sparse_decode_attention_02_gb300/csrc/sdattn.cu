@@ -432,11 +432,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int lane = threadIdx.x & 31;
     // this warp's Q fragment array (PAIR: its warp pair's token)
     const uint32_t qfrag = sbase + L::kQOff + (PAIR && warp < kConsumerWarps ? (warp >> 1) * L::kQBytes : 0);
-    // With PAIR, CTA u serves rows (token 2k, group g) and (token 2k + 1, g),
-    // u = k * G + g (one split); `row` is the first of them.
-    const int row = PAIR ? static_cast<int>((blockIdx.x / p.groups) * 2 * p.groups + blockIdx.x % p.groups)
-                         : static_cast<int>(blockIdx.x / p.splits);
-    const int split = PAIR ? 0 : static_cast<int>(blockIdx.x - row * p.splits);
+    // CTA (u, split) = blockIdx.x; with PAIR, unit u serves rows (token 2k,
+    // group g) and (token 2k + 1, g), u = k * G + g, and `row` is the first.
+    const int unit = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.splits));
+    const int split = static_cast<int>(blockIdx.x % static_cast<unsigned>(p.splits));
+    const int row = PAIR ? (unit / p.groups) * 2 * p.groups + unit % p.groups : unit;
 
     if (warp == kConsumerWarps) {          // the producer warp owns the pipeline barriers
         if (lane == 0) {
@@ -932,9 +932,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         const float mine = m_run[r];
         fac[r] = (Ls > 0.0f && mine != -INFINITY) ? fast_exp2(mine - M) / Ls : 0.0f;
-        if (p.splits > 1 && warp == 0 && t == 0 && h < p.heads && act)
-            p.lse[(static_cast<int64_t>(row) * p.splits + split) * p.heads + h] =
-                Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+        if (p.splits > 1 && warp == w0 && t == 0 && h < p.heads && act)   // PAIR: pair k is row + k G
+            p.lse[(static_cast<int64_t>(row + (PAIR ? (warp >> 1) * p.groups : 0)) * p.splits + split) *
+                      p.heads + h] = Ls > 0.0f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
     }
 
     // Scaled per-warp outputs into the (now idle) stage ring.
@@ -969,10 +969,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int r = e - k * total;
             const int h = r / kDim, d = r - h * kDim;
             const float v = (obuf[((2 * k) * kMaxHeads + h) * kObufStride + d] +
-                             obuf[((2 * k + 1) * kMaxHeads + h) * kObufStride + d]) *
-                            vfold * gam[k * kMaxHeads + h];
-            uint16_t *out = p.output + static_cast<int64_t>(row + k * p.groups) * p.o_s0;
-            out[static_cast<int64_t>(h) * p.o_s1 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+                             obuf[((2 * k + 1) * kMaxHeads + h) * kObufStride + d]) * vfold;
+            const int64_t orow = row + k * p.groups;
+            if (p.splits == 1) {
+                uint16_t *out = p.output + orow * p.o_s0;
+                out[static_cast<int64_t>(h) * p.o_s1 + d] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(v * gam[k * kMaxHeads + h]));
+            } else {                       // the combine kernel applies the gate
+                p.partial[(orow * p.splits + split) * p.heads * kDim + r] = v;
+            }
         }
     } else if (p.splits == 1) {
         if (!act && !p.clear_inactive)
@@ -1126,8 +1131,7 @@ sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, c
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(PAIR ? static_cast<unsigned>(prm.rows / 2)
-                            : static_cast<unsigned>(prm.rows) * static_cast<unsigned>(prm.splits));
+    cfg.gridDim = dim3(static_cast<unsigned>(PAIR ? prm.rows / 2 : prm.rows) * static_cast<unsigned>(prm.splits));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1398,8 +1402,8 @@ sda_status run_call(const Call &c)
     const int nr = windowed ? 0 : prm.num_regions;
     const bool full = piece == stage_tokens;
     // Window rows come in token pairs of one request (query_len even): one CTA
-    // streams the pair's union window once.
-    const bool pair = windowed && c.query_len % 2 == 0 && c.splits == 1;
+    // streams (its split's share of) the pair's union window once.
+    const bool pair = windowed && c.query_len % 2 == 0;
     if (fp8) {
         if (pair)
             return full ? launch<true, true, true, true>(tmap, prm, nr, s)
