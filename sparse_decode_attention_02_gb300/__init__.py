@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     read_errors,
     set_wait_limit_ns,
     sparse_decode_attention,
+    sparse_decode_attention_no_alloc,
     sparse_decode_select_regions,
     sparse_decode_splits,
     sparse_decode_summary_scores,

@@ -7,6 +7,7 @@ missing or fails to load, the call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import re
@@ -121,6 +122,34 @@ def _ref(d):
     return ctypes.byref(d) if d is not None else None
 
 
+def _device_of(*tensors, stream: torch.cuda.Stream | None = None) -> torch.device:
+    """The one CUDA device that every given tensor (None entries skipped) and
+    the stream belong to.  Raises ValueError for a CPU tensor or mixed devices,
+    before anything is allocated or launched: the kernels dereference every
+    pointer on that device."""
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if t.device.type != "cuda":
+            raise ValueError(f"sparse_decode: every tensor must be a CUDA tensor (got one on {t.device})")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"sparse_decode: tensors on {dev} and {t.device}; pass them all on one device")
+    if dev is None:
+        raise ValueError("sparse_decode: no tensor arguments")
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"sparse_decode: stream of {stream.device} for tensors on {dev}")
+    return dev
+
+
+def _current(dev: torch.device):
+    """Makes `dev` the current device for a library call (the library launches
+    on the current device)."""
+    return contextlib.nullcontext() if torch.cuda.current_device() == dev.index else torch.cuda.device(dev)
+
+
 def sparse_decode_splits(rows: int) -> int:
     return load().sparse_decode_splits(int(rows))
 
@@ -165,21 +194,24 @@ def sparse_decode_attention(query, cache, regions, block_table, positions, activ
     `splits=None` uses the library's split policy.  `k_scale`/`v_scale` are
     one-element float32 device tensors (python floats are uploaded)."""
     lib = load()
+    dev = _device_of(query, cache, regions, block_table, positions, active, output, gate, workspace,
+                     stream=stream)
     rows, heads = query.shape[0], query.shape[1]
     if splits is None:
         splits = lib.sparse_decode_splits(rows)
     need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
     if workspace is None:
-        workspace = default_workspace(query.device, need, stream)
-    ks, _keep_k = _scale_ptr(k_scale, query.device)
-    vs, _keep_v = _scale_ptr(v_scale, query.device)
+        workspace = default_workspace(dev, need, stream)
+    ks, _keep_k = _scale_ptr(k_scale, dev)
+    vs, _keep_v = _scale_ptr(v_scale, dev)
     descs = [describe(x) for x in (query, cache, regions, block_table, positions, active, output)]
     gd = describe(gate)
-    s = stream if stream is not None else torch.cuda.current_stream(query.device)
-    rc = lib.sparse_decode_attention(*[_ref(d) for d in descs], float(scale), int(query_len),
-                                     int(splits), ks, vs, _ref(gd), int(bool(clear_inactive)),
-                                     int(region_tokens), workspace.data_ptr(),
-                                     workspace.numel() * workspace.element_size(), s.cuda_stream)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with _current(dev):
+        rc = lib.sparse_decode_attention(*[_ref(d) for d in descs], float(scale), int(query_len),
+                                         int(splits), ks, vs, _ref(gd), int(bool(clear_inactive)),
+                                         int(region_tokens), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
 
@@ -197,20 +229,22 @@ def sparse_decode_swa_attention(query, cache, block_table, seq_lens, output, *, 
 
     `splits=None` uses the library's window split policy."""
     lib = load()
+    dev = _device_of(query, cache, block_table, seq_lens, output, gate, workspace, stream=stream)
     rows, heads = query.shape[0], query.shape[1]
     if splits is None:
         splits = lib.sparse_decode_swa_splits(rows, int(window))
     need = lib.sparse_decode_workspace_bytes(rows, heads, splits)
     if workspace is None:
-        workspace = default_workspace(query.device, need, stream)
-    ks, _keep_k = _scale_ptr(k_scale, query.device)
-    vs, _keep_v = _scale_ptr(v_scale, query.device)
+        workspace = default_workspace(dev, need, stream)
+    ks, _keep_k = _scale_ptr(k_scale, dev)
+    vs, _keep_v = _scale_ptr(v_scale, dev)
     descs = [describe(x) for x in (query, cache, block_table, seq_lens, output)]
     gd = describe(gate)
-    s = stream if stream is not None else torch.cuda.current_stream(query.device)
-    rc = lib.sparse_decode_swa_attention(*[_ref(d) for d in descs], float(scale), int(window), int(query_len),
-                                         int(splits), ks, vs, _ref(gd), workspace.data_ptr(),
-                                         workspace.numel() * workspace.element_size(), s.cuda_stream)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with _current(dev):
+        rc = lib.sparse_decode_swa_attention(*[_ref(d) for d in descs], float(scale), int(window),
+                                             int(query_len), int(splits), ks, vs, _ref(gd), workspace.data_ptr(),
+                                             workspace.numel() * workspace.element_size(), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
 
@@ -220,12 +254,14 @@ def sparse_decode_select_regions(scores, current, topk: int, regions=None, *, to
     """Region selection into `regions` ([rows, topk] int32, allocated if None);
     see include/sdattn.h for the rule.  Returns `regions`."""
     lib = load()
+    dev = _device_of(scores, current, topk_lengths, regions, stream=stream)
     if regions is None:
-        regions = torch.empty((scores.shape[0], int(topk)), dtype=torch.int32, device=scores.device)
-    s = stream if stream is not None else torch.cuda.current_stream(scores.device)
+        regions = torch.empty((scores.shape[0], int(topk)), dtype=torch.int32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
     d = [describe(x) for x in (scores, current, topk_lengths, regions)]
-    rc = lib.sparse_decode_select_regions(_ref(d[0]), _ref(d[1]), _ref(d[2]), int(topk), _ref(d[3]),
-                                          s.cuda_stream)
+    with _current(dev):
+        rc = lib.sparse_decode_select_regions(_ref(d[0]), _ref(d[1]), _ref(d[2]), int(topk), _ref(d[3]),
+                                              s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
     return regions
@@ -240,18 +276,21 @@ def sparse_decode_summary_scores(query, weights, summaries, block_table, seq_len
     optional `current` / `lengths` outputs; see include/sdattn.h.  Returns
     `scores`."""
     lib = load()
+    dev = _device_of(query, weights, summaries, block_table, seq_lens, scores, current, lengths, workspace,
+                     stream=stream)
     rows = query.shape[0] * query.shape[1]
     if scores is None:
         if n_cols is None:
             n_cols = block_table.shape[1] * int(block_size) // 8
-        scores = torch.empty((rows, int(n_cols)), dtype=torch.float32, device=query.device)
-    s = stream if stream is not None else torch.cuda.current_stream(query.device)
+        scores = torch.empty((rows, int(n_cols)), dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
     d = [describe(x) for x in (query, weights, summaries, block_table, seq_lens, scores, current, lengths)]
     ws = workspace.data_ptr() if workspace is not None else None
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib.sparse_decode_summary_scores(_ref(d[0]), _ref(d[1]), _ref(d[2]), _ref(d[3]), _ref(d[4]),
-                                          int(block_size), int(query_len), _ref(d[5]), _ref(d[6]),
-                                          _ref(d[7]), ws, wsb, s.cuda_stream)
+    with _current(dev):
+        rc = lib.sparse_decode_summary_scores(_ref(d[0]), _ref(d[1]), _ref(d[2]), _ref(d[3]), _ref(d[4]),
+                                              int(block_size), int(query_len), _ref(d[5]), _ref(d[6]),
+                                              _ref(d[7]), ws, wsb, s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
     return scores
@@ -261,9 +300,11 @@ def read_errors(workspace: torch.Tensor, clear: bool = False,
                 stream: torch.cuda.Stream | None = None) -> int:
     """Device error flags (FLAG_BOUNDS | FLAG_TIMEOUT) recorded in a workspace; synchronises."""
     lib = load()
-    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    dev = _device_of(workspace, stream=stream)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
     out = ctypes.c_uint32(0)
-    rc = lib.sparse_decode_read_errors(workspace.data_ptr(), ctypes.byref(out), int(clear), s.cuda_stream)
+    with _current(dev):
+        rc = lib.sparse_decode_read_errors(workspace.data_ptr(), ctypes.byref(out), int(clear), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
     return out.value
@@ -293,18 +334,20 @@ def sparse_decode_attention_no_alloc(query, cache, regions, block_table, positio
         fn.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                        ctypes.c_void_p, P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
         fn.restype = ctypes.c_int
-    rows = query.shape[0]
-    if splits is None:
-        splits = lib.sparse_decode_splits(rows)
     for x in (k_scale, v_scale):
         if x is not None and not isinstance(x, torch.Tensor):
             raise TypeError("k_scale / v_scale must be device tensors for the allocation-free call")
-    ks = k_scale.data_ptr() if k_scale is not None else None
-    vs = v_scale.data_ptr() if v_scale is not None else None
+    dev = _device_of(query, cache, regions, block_table, positions, active, output, gate, stream=stream)
+    rows = query.shape[0]
+    if splits is None:
+        splits = lib.sparse_decode_splits(rows)
+    ks, _keep_k = _scale_ptr(k_scale, dev)
+    vs, _keep_v = _scale_ptr(v_scale, dev)
     descs = [describe(x) for x in (query, cache, regions, block_table, positions, active, output)]
     gd = describe(gate)
-    s = stream if stream is not None else torch.cuda.current_stream(query.device)
-    rc = fn(*[_ref(d) for d in descs], float(scale), int(query_len), int(splits), ks, vs, _ref(gd),
-            int(bool(clear_inactive)), int(region_tokens), s.cuda_stream)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with _current(dev):
+        rc = fn(*[_ref(d) for d in descs], float(scale), int(query_len), int(splits), ks, vs, _ref(gd),
+                int(bool(clear_inactive)), int(region_tokens), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())

@@ -235,3 +235,44 @@ def test_summary_entry_validation(lib):
     z = dict(query=f.t(2, (0, G, 8, 256)), weights=f.t(6, (0, G, 8)), scores=f.t(6, (0, 128)),
              current=f.t(4, (0,)), lengths=f.t(4, (0,)))
     assert call(**z) == B.SDA_OK                                # no tokens: nothing to do
+
+
+def test_binding_rejects_host_tensors(lib):
+    """Host (CPU) tensors never reach the kernels: every Python entry raises before it
+    allocates a workspace or calls into the library."""
+    bf, i32 = torch.bfloat16, torch.int32
+    q, out = torch.zeros(4, 16, 192, dtype=bf), torch.zeros(4, 16, 192, dtype=bf)
+    cache = torch.zeros(8, 1, 16, 384, dtype=bf)
+    regions, table = torch.zeros(4, 2, dtype=i32), torch.zeros(4, 2, dtype=i32)
+    pos, act, seq = torch.zeros(4, dtype=i32), torch.ones(4, dtype=torch.bool), torch.ones(4, dtype=i32)
+    calls = [
+        lambda: sda.sparse_decode_attention(q, cache, regions, table, pos, act, out, scale=0.1, splits=1),
+        lambda: sda.sparse_decode_attention_no_alloc(q, cache, regions, table, pos, act, out, scale=0.1,
+                                                     splits=1),
+        lambda: sda.sparse_decode_swa_attention(q, cache, table, seq, out, scale=0.1, window=4, splits=1),
+        lambda: sda.sparse_decode_select_regions(torch.zeros(4, 8), pos, 2),
+        lambda: sda.sparse_decode_summary_scores(torch.zeros(4, 1, 8, 256, dtype=torch.uint8),
+                                                 torch.zeros(4, 1, 8), torch.zeros(16, 1, 256, dtype=torch.uint8),
+                                                 table, seq, block_size=16),
+        lambda: sda.read_errors(torch.zeros(256, dtype=torch.uint8)),
+    ]
+    before = dict(B._workspaces)
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
+    assert B._workspaces == before
+
+
+def test_binding_device_resolution():
+    """One device for all tensor arguments and the stream; None entries are skipped."""
+    from types import SimpleNamespace as NS
+    c0, c1 = torch.device("cuda", 0), torch.device("cuda", 1)
+    assert B._device_of(NS(device=c0), None, NS(device=c0)) == c0
+    with pytest.raises(ValueError, match="one device"):
+        B._device_of(NS(device=c0), NS(device=c1))
+    with pytest.raises(ValueError, match="stream"):
+        B._device_of(NS(device=c0), stream=NS(device=c1))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        B._device_of(NS(device=c0), NS(device=torch.device("meta")))
+    with pytest.raises(ValueError, match="no tensor"):
+        B._device_of(None)
