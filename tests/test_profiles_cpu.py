@@ -1,8 +1,9 @@
-"""The committed ncu traffic records describe the kernels as they are now.
+"""The committed ncu records and summaries describe the kernels as they are now.
 
-bench.py scales each record's DRAM bytes to the timed launch and reports
-null once the kernel source no longer matches the recorded hash; this test
-makes a kernel change without a fresh capture fail loudly instead."""
+bench.py scales each traffic record's DRAM bytes to the timed launch and
+reports null once the kernel source no longer matches the recorded hash; these
+tests make a kernel change without fresh captures fail loudly instead, for the
+traffic records and for every summary under profiles/."""
 import hashlib
 import os
 
@@ -45,3 +46,20 @@ def test_index_traffic_accounting():
     expect = 11 * 2 * 256 + 6 * 10 * 4 + 3 * 2 * 8 * 260 + 6 * 4 + 3 * 4
     assert bench.index_traffic(w) == expect
     assert bench.index_traffic(w, with_outputs=True) == expect + 6 * 8
+
+
+def test_profile_summaries_name_current_sources():
+    """Every ncu summary states the kernel-source hash(es) it was taken on, and each is the
+    hash of a current source: a kernel change without fresh captures fails here."""
+    import glob
+    import re
+    csrc = os.path.join(ROOT, "sparse_decode_attention_02_gb300", "csrc")
+    current = {hashlib.sha256(open(os.path.join(csrc, n), "rb").read()).hexdigest()[:16]: n
+               for n in ("sdattn.cu", "sda_index.cu", "sda_select.cu")}
+    summaries = sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md")))
+    assert summaries
+    for path in summaries:
+        hashes = set(re.findall(r"\b[0-9a-f]{16}\b", open(path).read()))
+        assert hashes, f"{os.path.basename(path)} names no kernel-source hash"
+        stale = sorted(h for h in hashes if h not in current)
+        assert not stale, f"{os.path.basename(path)}: stale source hash(es) {stale}; re-capture"
