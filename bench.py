@@ -700,11 +700,14 @@ def run_index(args, dev, world, rank, kind):
         for _ in range(3):
             e2e_step()
         torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
         torch.cuda.synchronize()
-        dt = time.perf_counter() - t0
+        dt = max_over_ranks(time.perf_counter() - t0, dev)      # slowest replica sets the job time
         line["e2e"] = {"value": iw.rows * e2e_steps * world / dt, "unit": "rows/s",
                        "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
                        "d2h_bytes_per_step": host_out.numel() * host_out.element_size(),
@@ -900,7 +903,7 @@ def main():
                 scratch.zero_()
             e2e_step()
         torch.cuda.synchronize()
-        e2e_s = time.perf_counter() - t0
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dev)   # slowest replica sets the job time
         line["e2e"] = {"value": w.rows * e2e_steps * world / e2e_s, "unit": "rows/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "note": "host wall clock; includes the L2 flush when flushing"}
