@@ -30,9 +30,10 @@ def mini(**changes):
     return inputs.make_workload(inputs.scaled("swa", **changes), DEV, fill="all")
 
 
-def test_swa_workload_sampled_rows():
+@pytest.mark.parametrize("splits", [None, 2])    # the policy (one split), and token pairs with partials
+def test_swa_workload_sampled_rows(splits):
     w = inputs.make_workload("swa", DEV)
-    out, flags = run_swa(w)
+    out, flags = run_swa(w, splits=splits)
     assert flags == 0
     assert torch.isfinite(out.float()).all()
     rows = sample_rows(w, 128)
