@@ -12,11 +12,12 @@
 // One CTA of 256 threads per row (4 per SM), scores compared as
 // order-preserving 32-bit keys; the row is prefetched into L2 at entry.
 //   Fast path (rows of up to 64K candidates): a low threshold is estimated
-//   from a 2048-score sample so that about 2 * topk scores pass it; one
-//   streaming pass (a plain float comparison against the threshold's
-//   smallest passing value) keeps the passing (key, id) pairs in shared memory; an
-//   exact radix select on that buffer gives the last kept key; bitmaps over
-//   the ids give the lowest-id ties and the ascending output.
+//   from a 2048-score sample so that the topk best scores pass it with a
+//   margin of five binomial standard deviations; one streaming pass (a plain
+//   float comparison against the threshold's smallest passing value) keeps
+//   the passing (key, id) pairs in shared memory; an exact radix select on
+//   that buffer gives the last kept key; bitmaps over the ids give the
+//   lowest-id ties and the ascending output.
 //   Fallback (buffer overflow or underflow, longer rows): an exact 4-pass
 //   radix select that streams the row each pass, then an ordered compaction.
 #include <cuda_runtime.h>
@@ -285,7 +286,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) sda_select_kernel(const __grid
             for (int j = tid; j < kSample; j += kSelThreads)
                 sh.a.sample[j] = score_key(sc[static_cast<int64_t>(j) * len / kSample]);
             __syncthreads();
-            const int r = min(kSample, static_cast<int>((2ll * k * kSample + cand - 1) / cand) + 32);
+            // Sample rank of the bound: the sample's expected count of the row's
+            // top k (a binomial mean mu) plus five standard deviations and a
+            // constant, so that fewer than k candidates reach the bound only
+            // with probability ~1e-7 (the exact fallback then takes the row).
+            const float mu = static_cast<float>(k) * kSample / static_cast<float>(cand);
+            const int r = min(kSample, static_cast<int>(mu + 5.0f * sqrtf(mu)) + 17);
             int unused;
             t_lo = select_shared(sh, sh.a.sample, kSample, r, &unused, 2);   // 16-bit lower bound
         }
