@@ -56,8 +56,9 @@ def test_select_matches_oracle(rows, n, topk, ties):
     assert np.array_equal(got, ref)
 
 
-def test_select_large_decode_rows():
-    sw = inputs.make_select_workload(DEV)
+@pytest.mark.parametrize("topk", [1024, 2048])
+def test_select_large_decode_rows(topk):
+    sw = inputs.make_select_workload(DEV, topk=topk)
     got, ref = select_both(sw.scores, sw.current, sw.topk, sw.lengths)
     assert np.array_equal(got, ref)
     assert (got[:, 0] == sw.current.cpu().numpy()).all()
