@@ -192,11 +192,12 @@ def test_decode_chain_scores_select_attention():
     assert err <= 2e-2, err
 
 
-def test_decode_chain_full_size_sampled():
+@pytest.mark.parametrize("query_len", [1, 2])    # 2: speculative decode, two tokens per request
+def test_decode_chain_full_size_sampled(query_len):
     """The whole decode step at full size (512 requests x 4 groups, contexts
     128K-256K, top-1024 of 8-token regions, FP8 cache) in the launch
     configuration the benchmark times; sampled requests checked step by step."""
-    ch = inputs.make_decode_chain(DEV)
+    ch = inputs.make_decode_chain(DEV, query_len=query_len)
     iw = ch.index
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
     scores = torch.empty((iw.rows, iw.n_cols), device=DEV)
@@ -215,7 +216,8 @@ def test_decode_chain_full_size_sampled():
     torch.cuda.synchronize()
     assert sda.read_errors(ws) == 0
     reqs = [5, 300]
-    rows = [r * iw.groups + g for r in reqs for g in range(iw.groups)]
+    ql, G = iw.query_len, iw.groups
+    rows = [(r * ql + t) * G + g for r in reqs for t in range(ql) for g in range(G)]
     sub = inputs.index_host_subset(iw, reqs)
     check((scores[rows].cpu().numpy(), cur[rows].cpu().numpy(), lens[rows].cpu().numpy()),
           run_oracle(sub), run_oracle(sub, absolute=True)[0])
