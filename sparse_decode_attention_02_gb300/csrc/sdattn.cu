@@ -405,10 +405,11 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
 // ---------------------------------------------------------------------------
 
 // FULL: a piece fills a whole stage (P = slots per stage), so the stage
-// layout is a compile-time [band][slot] one.  PAIR (window mode, one split):
-// a CTA serves two consecutive query tokens of a request and group, whose
-// windows are one token apart; the producer streams their union once, each
-// warp pair computes one token over every stage.
+// layout is a compile-time [band][slot] one.  PAIR (window mode, even
+// query_len): a CTA serves two consecutive query tokens of a request and
+// group, whose windows are one token apart; the producer streams (its split's
+// share of) their union once, each warp pair computes one token over every
+// stage and writes that token's row (output, or partial and LSE).
 template <bool FP8, bool WINDOW, bool FULL, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 2)
     sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
