@@ -116,6 +116,8 @@ size_t sparse_decode_workspace_bytes(int rows, int heads, int splits);
  *                head h of row r is multiplied by bf16(sigmoid(gate[r/G,
  *                (r%G)*H + h])) computed in fp32 (the page's `_gate`).
  *   clear_inactive  nonzero: inactive rows are written as +0.0; zero: left as is.
+ *                (The adapter page's decode path passes clear_inactive || gate,
+ *                so gated layers always clear; that policy is the caller's.)
  *   region_tokens   RT; 0 means RT = B.  min(RT, B, 64) must be a multiple of 8
  *                and divide both RT and B.
  *   workspace    device buffer of >= sparse_decode_workspace_bytes(rows, H,
