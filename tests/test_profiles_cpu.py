@@ -63,3 +63,40 @@ def test_profile_summaries_name_current_sources():
         assert hashes, f"{os.path.basename(path)} names no kernel-source hash"
         stale = sorted(h for h in hashes if h not in current)
         assert not stale, f"{os.path.basename(path)}: stale source hash(es) {stale}; re-capture"
+
+
+def test_split_traffic_accounting():
+    """Algorithmic bytes of the sparse and window paths on a hand-counted workload: one request,
+    2 tokens at positions 40 and 41, 2 groups, 16-token blocks = regions, 4 heads, bf16."""
+    import numpy as np
+    import torch
+    import bench
+    from sparse_decode_attention_02_gb300 import inputs
+    cfg = inputs.Config("hand", requests=1, query_len=2, groups=2, heads=4, block=16, region_tokens=16,
+                        num_regions=3, ctx=(42, 42))
+    i32 = lambda a: torch.tensor(a, dtype=torch.int32)
+    w = inputs.Workload(cfg, torch.zeros(4, 4, 192, dtype=torch.bfloat16),
+                        torch.zeros(4, 2, 16, 384, dtype=torch.bfloat16),
+                        i32([[0, 2, -1], [1, 2, 5], [2, -1, -1], [0, 1, 2]]), i32([[0, 1, 2, 3]]),
+                        i32([40, 40, 41, 41]), torch.tensor([1, 1, 1, 0], dtype=torch.uint8), None,
+                        None, None, 192 ** -0.5, None, np.zeros((0, 2), np.int64), i32([42]))
+    # row 0: region 0 (16) + region 2 (tokens 32..40: 9); row 1: 16 + 9, region 5 is in the future;
+    # row 2: region 2 up to 41 (10); row 3 is inactive
+    assert bench.visible_tokens(w).tolist() == [25, 25, 10, 0]
+    # distinct tokens per (request, group): group 0 rows 0 and 2 -> regions {0, 2} up to 41: 16 + 10;
+    # group 1 row 1 only -> regions {1, 2} up to 40: 16 + 9
+    assert bench.unique_kv_bytes(w) == 51 * 384 * 2
+    per_row = 4 * 192 * 2 * 2 + 3 * 4 + 8                       # Q + out, region ids, position+flag
+    table = (2 + 2 + 1) * 4                                     # ceil(visible / 16) entries per row
+    assert bench.traffic(w, 1) == (60 * 384 * 2, 60 * 384 * 2 + 3 * per_row + table)
+    partials = 3 * 2 * 4 * 193 * 4 * 2                          # active rows x S x H x (O + LSE), w + r
+    assert bench.traffic(w, 2)[1] == 60 * 384 * 2 + 3 * per_row + table + partials
+    # window mode, window 8 (window rows have no active flag: every row runs): each row sees
+    # 8 tokens; the union per (request, group) is 33..41, 9 tokens, for both groups
+    import dataclasses
+    ww = dataclasses.replace(w, config=dataclasses.replace(cfg, window=8, num_regions=0),
+                             regions=torch.zeros(4, 0, dtype=torch.int32),
+                             active=torch.ones(4, dtype=torch.uint8))
+    assert bench.visible_tokens(ww).tolist() == [8, 8, 8, 8]
+    assert bench.unique_kv_bytes(ww) == 18 * 384 * 2
+    assert bench.traffic(ww, 1) == (32 * 384 * 2, 18 * 384 * 2 + 4 * (4 * 192 * 4 + 8) + 4 * 4)
