@@ -276,3 +276,22 @@ def test_binding_device_resolution():
         B._device_of(NS(device=c0), NS(device=torch.device("meta")))
     with pytest.raises(ValueError, match="no tensor"):
         B._device_of(None)
+
+
+def test_swa_splits_policy(lib):
+    """The window split policy as include/sdattn.h states it: the sparse path's split count for
+    the row count (its golden truth table), halved while a split would cover fewer than 256
+    window tokens."""
+    table = []
+    with open(os.path.join(GOLDEN, "sparse_decode_splits.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].split()
+            if line:
+                table.append(tuple(int(x) for x in line))
+    for lo, hi, s in table:
+        for rows in sorted({lo, hi, (lo + hi) // 2}):
+            for window in (1, 100, 255, 256, 257, 511, 512, 1024, 2048, 4096, 8192, 1 << 20):
+                want = s
+                while want > 1 and window // want < 256:
+                    want //= 2
+                assert sda.sparse_decode_swa_splits(rows, window) == want, (rows, window)
