@@ -134,7 +134,11 @@ size_t sparse_decode_workspace_bytes(int rows, int heads, int splits);
  *
  * FP8 note: the kernels convert E4M3 to fp16 exactly; the two NaN codes
  * (S.1111.111) are not meaningful cache contents and are not special-cased.
- * The FP8 path multiplies q in fp16, so |q| must stay below 65504.
+ * The FP8 path multiplies in fp16: each row's q is first scaled by a power of
+ * two that puts its largest |q| in [2^14, 2^15), and the factor is undone in
+ * the fp32 logit scale, so any finite bf16 query is taken at full precision
+ * (values more than 2^31 below the row's largest lose low bits) as long as
+ * the logits scale * q.k * k_scale fit in fp32.
  */
 sda_status sparse_decode_attention(const sda_tensor *query, const sda_tensor *cache,
                                    const sda_tensor *regions, const sda_tensor *block_table,
@@ -275,24 +279,29 @@ void sparse_decode_set_wait_limit_ns(uint64_t ns);
  *
  * For callers that cannot obtain device memory for a workspace: plugin or
  * FFI hosts that are handed tensor pointers by another runtime but no
- * allocator, and code running where a cudaMalloc would synchronise the device
- * or break a stream capture in progress.  Arguments and results are those of
- * sparse_decode_attention without `workspace` / `workspace_bytes`: the
- * scratch (flag header, split partials and LSEs) lives in an 8 MiB static
- * device array inside the library, which every GPU that loads the library
- * holds until the process exits.
+ * allocator, and code that must not call cudaMalloc while other work is in
+ * flight (an allocation can synchronise the device).  Arguments and results
+ * are those of sparse_decode_attention without `workspace` /
+ * `workspace_bytes`: the scratch (flag header, split partials and LSEs) lives
+ * in an 8 MiB static device array inside the library, which every GPU that
+ * loads the library holds until the process exits.
  *   - Limit: sparse_decode_workspace_bytes(rows, H, splits) must be at most
  *     8 MiB (8388608), else SDA_ERR_WORKSPACE is returned and nothing is
  *     enqueued.  splits == 1 needs 256 bytes, so any row count fits; with
- *     16 heads, rows * splits up to 679 fits.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture on the device.
+ *     16 heads, rows * splits up to 679 fits.  Arguments outside the contract
+ *     get the statuses of sparse_decode_attention, checked first, also with
+ *     nothing enqueued.
+ *   - The first call on a device (of this function or of
+ *     sparse_decode_no_alloc_read_errors) looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and zeroes its flag
+ *     header with an async memset on `stream`; make that first call before
+ *     any stream capture on the device.
  *   - Every call on a device shares the one array, which keeps the previous
  *     call's contents.  Calls whose kernels overlap on the GPU (different
  *     streams, no ordering between them) race on it: serialise them.
- *   - Each call clears the flag header (an async memset on `stream`); device
- *     flags of this variant are not reported to the caller.
+ *   - Device flags (SDA_FLAG_*) collect in the array's header over calls, as
+ *     in a caller's workspace; read and clear them with
+ *     sparse_decode_no_alloc_read_errors.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
  */
 sda_status sparse_decode_attention_no_alloc(const sda_tensor *query, const sda_tensor *cache,
@@ -302,6 +311,16 @@ sda_status sparse_decode_attention_no_alloc(const sda_tensor *query, const sda_t
                                             int splits, const float *k_scale, const float *v_scale,
                                             const sda_tensor *gate, int clear_inactive,
                                             int region_tokens, void *stream);
+
+/*
+ * The device flags of sparse_decode_attention_no_alloc on the current device
+ * (the page has no counterpart): as sparse_decode_read_errors on the static
+ * array's header.  Synchronises `stream`, which must be ordered after the
+ * calls whose flags are wanted; with `clear` the header is zeroed afterwards.
+ * Returns SDA_ERR_INVALID for a NULL `flags`, SDA_ERR_CUDA if a CUDA call
+ * failed.
+ */
+sda_status sparse_decode_no_alloc_read_errors(uint32_t *flags, int clear, void *stream);
 
 /* A static description of a status code. */
 const char *sparse_decode_status_string(int status);

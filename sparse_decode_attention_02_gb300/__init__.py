@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     declared_functions,
     default_workspace,
     load,
+    no_alloc_read_errors,
     read_errors,
     set_wait_limit_ns,
     sparse_decode_attention,

@@ -73,6 +73,13 @@ def _declare(lib):
     lib.sparse_decode_read_errors.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32),
                                               ctypes.c_int, ctypes.c_void_p]
     lib.sparse_decode_read_errors.restype = ctypes.c_int
+    lib.sparse_decode_attention_no_alloc.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, P,
+                                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.sparse_decode_attention_no_alloc.restype = ctypes.c_int
+    lib.sparse_decode_no_alloc_read_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
+                                                       ctypes.c_void_p]
+    lib.sparse_decode_no_alloc_read_errors.restype = ctypes.c_int
     lib.sparse_decode_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.sparse_decode_set_wait_limit_ns.restype = None
     lib.sparse_decode_status_string.argtypes = [ctypes.c_int]
@@ -325,15 +332,12 @@ def sparse_decode_attention_no_alloc(query, cache, regions, block_table, positio
     """The allocation-free C entry point: same contract as sparse_decode_attention
     but its scratch is the library's static 8 MiB device array (no workspace
     argument).  For callers that cannot allocate device memory; calls that
-    overlap on the GPU race on the shared array.  `k_scale`/`v_scale` must be
-    device tensors here (uploading a python float would allocate)."""
+    overlap on the GPU race on the shared array.  Device flags collect in the
+    array until read with `no_alloc_read_errors(clear=True)`.
+    `k_scale`/`v_scale` must be device tensors here (uploading a python float
+    would allocate)."""
     lib = load()
     fn = lib.sparse_decode_attention_no_alloc
-    if not fn.argtypes:
-        P = ctypes.POINTER(SdaTensor)
-        fn.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
-                       ctypes.c_void_p, P, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
-        fn.restype = ctypes.c_int
     for x in (k_scale, v_scale):
         if x is not None and not isinstance(x, torch.Tensor):
             raise TypeError("k_scale / v_scale must be device tensors for the allocation-free call")
@@ -351,3 +355,27 @@ def sparse_decode_attention_no_alloc(query, cache, regions, block_table, positio
                 int(bool(clear_inactive)), int(region_tokens), s.cuda_stream)
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+
+
+def no_alloc_read_errors(clear: bool = False, stream: torch.cuda.Stream | None = None,
+                         device: torch.device | int | None = None) -> int:
+    """Device error flags (FLAG_BOUNDS | FLAG_TIMEOUT) that the allocation-free
+    entry point's calls on `device` (default: the current one) have collected
+    in its static array; synchronises `stream`, optionally clears them."""
+    lib = load()
+    if device is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    elif isinstance(device, int):
+        dev = torch.device("cuda", device)
+    else:
+        dev = torch.device(device)
+        dev = torch.device("cuda", dev.index if dev.index is not None else torch.cuda.current_device())
+    if stream is not None and stream.device != dev:
+        raise ValueError(f"sparse_decode: stream of {stream.device} for {dev}")
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    out = ctypes.c_uint32(0)
+    with _current(dev):
+        rc = lib.sparse_decode_no_alloc_read_errors(ctypes.byref(out), int(clear), s.cuda_stream)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
+    return out.value

@@ -326,6 +326,24 @@ __device__ __forceinline__ float gate_factor(uint16_t g_bits)
     return __bfloat162float(__float2bfloat16_rn(sig));
 }
 
+// FP8 path: the power-of-two exponent e by which a consumer warp scales its
+// token's q before the fp16 MMA, from the per-warp maxima of the bf16 bit
+// patterns (|q|) that the consumers left in ctl[4..7]: e puts the largest |q|
+// in [2^14, 2^15) (14 - unbiased exponent, subnormals as the smallest
+// exponent), clamped so that 2^e and 2^-e stay normal fp32 numbers; 0 for an
+// all-zero q and on the bf16 path.
+template <bool FP8, bool PAIR>
+__device__ __forceinline__ int q_prescale_exp(const volatile int *ctl, int warp)
+{
+    if constexpr (!FP8) {
+        return 0;
+    } else {
+        const int m = PAIR ? max(ctl[4 + (warp & 2)], ctl[5 + (warp & 2)])
+                           : max(max(ctl[4], ctl[5]), max(ctl[6], ctl[7]));
+        return m ? min(126, max(-126, 141 - max(1, m >> 7))) : 0;
+    }
+}
+
 // Token slot of k-index n (0..7) inside an 8-slot group.  Pairs of fragment
 // columns (2p, 2p+1) map to slots (p, p+4) so that the eight 16-byte K reads
 // of one shared-memory phase hit eight different swizzled chunks.
@@ -541,23 +559,48 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int qrow = PAIR ? row + (warp >> 1) * p.groups : row;   // PAIR: the warp pair's token
         const uint16_t *q0 = p.query + static_cast<int64_t>(qrow) * p.q_s0;
         const int m0 = g, m1 = g + 8;
-#pragma unroll
-        for (int kk = PAIR ? (warp & 1) : warp; kk < 12; kk += PAIR ? 2 : kConsumerWarps) {
-            int d0;
+        const int kk0 = PAIR ? (warp & 1) : warp;
+        constexpr int kKStride = PAIR ? 2 : kConsumerWarps;
+        auto dim0 = [&](int kk) {
             if constexpr (FP8)
-                d0 = 64 * (kk >> 2) + 16 * t + 4 * (kk & 3);
+                return 64 * (kk >> 2) + 16 * t + 4 * (kk & 3);
             else
-                d0 = 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * t + 4 * (kk & 1);
+                return 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * t + 4 * (kk & 1);
+        };
+        auto q_bits = [&](int m, int d) -> uint32_t {
+            return act && m < p.heads ? q0[static_cast<int64_t>(m) * p.q_s1 + d] : 0u;
+        };
+        if constexpr (FP8) {
+            // The fp16 MMA takes q in fp16, whose range is far narrower than
+            // bf16's.  Scale the row's q by 2^e so that its largest |q| lands
+            // in [2^14, 2^15): every bf16 value within 2^31 of that maximum is
+            // then exact in fp16, and 2^-e is folded back into the logit
+            // scale, so the logits are those of the unscaled q up to fp32
+            // rounding.  The maximum runs over all of the token's heads and
+            // dims (this warp's k-steps, then the warps holding the token).
+            uint32_t mx = 0;
+#pragma unroll
+            for (int kk = kk0; kk < 12; kk += kKStride) {
+                const int d0 = dim0(kk);
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    mx = max(mx, max(q_bits(m0, d0 + e), q_bits(m1, d0 + e)) & 0x7FFFu);
+            }
+            mx = __reduce_max_sync(~0u, mx);
+            if (lane == 0)
+                ctl[4 + warp] = static_cast<int>(mx);
+            consumer_bar();
+        }
+        const float qs = __int_as_float((127 + q_prescale_exp<FP8, PAIR>(ctl, warp)) << 23);   // exact
+#pragma unroll
+        for (int kk = kk0; kk < 12; kk += kKStride) {
+            const int d0 = dim0(kk);
             float a[2][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                const int m = r ? m1 : m0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float v = m < p.heads ? bf16_bits_to_float(q0[static_cast<int64_t>(m) * p.q_s1 + d0 + e])
-                                                : 0.0f;
-                    a[r][e] = act ? v : 0.0f;
-                }
+                for (int e = 0; e < 4; ++e)
+                    a[r][e] = bf16_bits_to_float(static_cast<uint16_t>(q_bits(r ? m1 : m0, d0 + e))) * qs;
             }
             const uint32_t addr = qfrag + (kk * 32 + lane) * 16;
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
@@ -693,18 +736,35 @@ __global__ void __launch_bounds__(kThreads, 2)
                 mbar_arrive(full_bar + 8 * stage);
                 ++issued;
             }
-            // Let every copy this CTA started land before any thread can exit.
+            // Let every copy this CTA started land before the consumers reuse
+            // the ring for the epilogue and before any thread can exit.
+            bool drained = true;
             for (int k = issued > T::kStages ? issued - T::kStages : 0; k < issued; ++k)
-                mbar_wait(full_bar + 8 * (k % T::kStages), static_cast<uint32_t>(k / T::kStages) & 1u,
-                          kDrainLimitNs);
+                drained = mbar_wait(full_bar + 8 * (k % T::kStages), static_cast<uint32_t>(k / T::kStages) & 1u,
+                                    kDrainLimitNs) && drained;
+            if (!drained)
+                atomicOr(p.flags, SDA_FLAG_TIMEOUT);
+            ctl[3] = drained ? 0 : 1;
         }
+        __syncwarp();
+        asm volatile("bar.arrive 3, %0;" ::"n"(kThreads) : "memory");   // ring drained (or given up)
         return;
     }
 
     // ---- Consumers.
     const float kfold = FP8 ? __ldg(p.k_scale) : 1.0f;
     const float vfold = FP8 ? __ldg(p.v_scale) : 1.0f;
-    const float sl2 = p.scale * kLog2e * kfold;
+    // Logit scale in log2 units.  FP8: with the q prescale undone (exact); it
+    // passes through shared memory, which keeps the FP8 variants free of
+    // register spills.
+    float sl2 = p.scale * kLog2e * kfold;
+    float *sl2_smem = reinterpret_cast<float *>(ctl + 8 + warp);
+    if constexpr (FP8) {
+        if (lane == 0)
+            *sl2_smem = sl2 * __int_as_float((127 - q_prescale_exp<FP8, PAIR>(ctl, warp)) << 23);
+        __syncwarp();
+        sl2 = *sl2_smem;
+    }
 
     float o[24][4];
 #pragma unroll
@@ -911,7 +971,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             p.gate ? gate_factor(p.gate[(tok + k) * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
                    : 1.0f;
     }
-    consumer_bar();
+    // Every consumer's statistics are in shared memory, and the producer has
+    // seen every copy it issued land (after a timed-out wait some may still
+    // have been in flight), so the ring is free for the epilogue buffer.  If
+    // the producer's drain itself ran out, the ring may still receive bytes:
+    // the row is already flagged SDA_FLAG_TIMEOUT, and nothing more is written.
+    asm volatile("bar.sync 3, %0;" ::"n"(kThreads) : "memory");
+    if (ctl[3])
+        return;
 
     float fac[2];
 #pragma unroll
@@ -1234,7 +1301,9 @@ struct Call {
     void *stream;
 };
 
-sda_status run_call(const Call &c)
+// With check_only, returns after the argument contract (everything but the
+// workspace) without touching the GPU.
+sda_status run_call(const Call &c, bool check_only = false)
 {
     const bool windowed = c.window > 0;
     const sda_tensor *query = c.query, *cache = c.cache, *block_table = c.block_table, *output = c.output;
@@ -1318,6 +1387,8 @@ sda_status run_call(const Call &c)
         (cache->stride[2] * elt) % 16 != 0 || cache->stride[0] <= 0 || cache->stride[1] <= 0 ||
         cache->stride[2] <= 0)
         return SDA_ERR_UNSUPPORTED;
+    if (check_only)
+        return SDA_OK;
     const size_t need = sparse_decode_workspace_bytes(static_cast<int>(rows), static_cast<int>(heads), c.splits);
     if (!c.workspace || reinterpret_cast<uintptr_t>(c.workspace) % 256 != 0 || c.workspace_bytes < need)
         return SDA_ERR_WORKSPACE;
@@ -1471,9 +1542,9 @@ sda_status sparse_decode_swa_attention(const sda_tensor *query, const sda_tensor
 //
 // For callers that hold device pointers to their tensors but have no way to
 // obtain more device memory: plugin or FFI hosts that receive buffers from
-// another runtime without an allocator handle, and code running where a
-// cudaMalloc would synchronise the device or break a stream capture in
-// progress.  The split-KV scratch (flag header, fp32 partials and LSEs) lives
+// another runtime without an allocator handle, and code that must not call
+// cudaMalloc while other work is in flight (an allocation can synchronise the
+// device).  The split-KV scratch (flag header, fp32 partials and LSEs) lives
 // in the fixed file-scope array below instead of a caller-supplied buffer.
 // Every GPU that loads this library holds the array until the process exits.
 // ---------------------------------------------------------------------------
@@ -1485,6 +1556,29 @@ static __device__ __align__(256) unsigned char g_sda_static_scratch[kStaticScrat
 std::mutex g_static_scratch_mu;
 void *g_static_scratch_ptr[256] = {};   // device address of the array, per device
 
+// The array's device address on the current device.  The first use on a device
+// looks it up (cudaGetSymbolAddress, with that device current) and zeroes the
+// flag header on `stream`; later uses only read the cached address.
+sda_status static_scratch(cudaStream_t stream, void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SDA_ERR_CUDA;
+    if (dev < 0 || dev >= 256)
+        return SDA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_sda_static_scratch) != cudaSuccess || !ptr)
+            return SDA_ERR_CUDA;
+        if (cudaMemsetAsync(ptr, 0, kHeaderBytes, stream) != cudaSuccess)
+            return SDA_ERR_CUDA;
+        g_static_scratch_ptr[dev] = ptr;
+    }
+    *out = g_static_scratch_ptr[dev];
+    return SDA_OK;
+}
+
 }  // namespace
 
 extern "C" sda_status sparse_decode_attention_no_alloc(
@@ -1493,37 +1587,35 @@ extern "C" sda_status sparse_decode_attention_no_alloc(
     const sda_tensor *output, float scale, int query_len, int splits, const float *k_scale,
     const float *v_scale, const sda_tensor *gate, int clear_inactive, int region_tokens, void *stream)
 {
-    if (!query || query->ndim != 3)
+    if (!regions || !positions || !active)
         return SDA_ERR_INVALID;
-    // Size check first: the shared array must hold this call's scratch.
+    Call c{query, cache, regions, block_table, positions, active, nullptr, output, gate,
+           scale, query_len, splits, clear_inactive, region_tokens, 0,
+           k_scale, v_scale, nullptr, 0, stream};
+    // The argument contract first, with the statuses of the regular entry
+    // point; then the one status of this variant: scratch beyond the array.
+    if (const sda_status st = run_call(c, true))
+        return st;
     const size_t need = sparse_decode_workspace_bytes(static_cast<int>(query->shape[0]),
                                                       static_cast<int>(query->shape[1]), splits);
-    if (query->shape[0] < 0 || query->shape[0] > INT32_MAX || need == 0 || need > kStaticScratchBytes)
+    if (need == 0 || need > kStaticScratchBytes)
         return SDA_ERR_WORKSPACE;
-    // Once per device, with that device current: the array's device address.
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return SDA_ERR_CUDA;
-    if (dev < 0 || dev >= 256)
-        return SDA_ERR_UNSUPPORTED;
-    void *scratch = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_static_scratch_mu);
-        if (!g_static_scratch_ptr[dev]) {
-            void *p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_sda_static_scratch) != cudaSuccess || !p)
-                return SDA_ERR_CUDA;
-            g_static_scratch_ptr[dev] = p;
-        }
-        scratch = g_static_scratch_ptr[dev];
-    }
-    // The array keeps the previous call's contents: the kernels only OR into
-    // the flag header, so it starts every call at zero.  Partials and LSEs are
-    // written before they are read and need no clearing.
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (query->shape[0] > 0 && cudaMemsetAsync(scratch, 0, kHeaderBytes, s) != cudaSuccess)
-        return SDA_ERR_CUDA;
-    return sparse_decode_attention(query, cache, regions, block_table, positions, active, output, scale,
-                                   query_len, splits, k_scale, v_scale, gate, clear_inactive,
-                                   region_tokens, scratch, kStaticScratchBytes, stream);
+    if (const sda_status st = static_scratch(s, &c.workspace))
+        return st;
+    // The kernels only OR into the flag header, so flags collect over calls
+    // until sparse_decode_no_alloc_read_errors clears them; partials and LSEs
+    // are written before they are read and need no clearing.
+    c.workspace_bytes = kStaticScratchBytes;
+    return run_call(c);
+}
+
+extern "C" sda_status sparse_decode_no_alloc_read_errors(uint32_t *flags, int clear, void *stream)
+{
+    if (!flags)
+        return SDA_ERR_INVALID;
+    void *scratch = nullptr;
+    if (const sda_status st = static_scratch(static_cast<cudaStream_t>(stream), &scratch))
+        return st;
+    return sparse_decode_read_errors(scratch, flags, clear, stream);
 }

@@ -312,6 +312,25 @@ def test_bad_indices_are_flagged_not_faulted():
     assert torch.isfinite(out.float()).all()
 
 
+@pytest.mark.parametrize("splits", [1, 2])
+def test_fp8_query_of_any_bf16_magnitude(splits):
+    """The FP8 path multiplies in fp16, whose range bf16 queries exceed: rows whose q sits
+    around 1e5 (past fp16's 65504), around 1e-6 (below fp16's normal range), or mixes 3e4
+    with 1e-3 inside one head must still match the oracle, with no NaN or Inf."""
+    w = mini("fp8", requests=6, ctx=(2000, 6000), gate=True)
+    q = w.query.float()
+    q[0::4] *= 1e5
+    q[1::4] *= 1e-6
+    q[2::4, :, :96] *= 3e4
+    q[2::4, :, 96:] *= 1e-3
+    w.query.copy_(q.to(torch.bfloat16))
+    assert w.query[0::4].float().abs().max().item() > 65504
+    out, flags = run(w, splits=splits)
+    assert flags == 0
+    rows = list(range(w.rows))
+    check(w, out, oracle_rows(w, rows), rows)
+
+
 def test_deterministic_and_graph_capturable():
     w = mini("fp8", requests=8, ctx=(2000, 6000))
     S = sda.sparse_decode_splits(w.rows)
