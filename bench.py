@@ -13,6 +13,7 @@ workload (rows are independent; no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -47,6 +48,8 @@ def parse():
     ap.add_argument("--ctx", type=int, nargs=2, default=None, help="context range override (profiling)")
     ap.add_argument("--query-len", type=int, default=None,
                     help="tokens per request for the index and decode configs (speculative decode)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the forced split counts and the small decode workloads after the headline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=None)
@@ -94,6 +97,15 @@ def describe(cfg, w, splits):
         "inactive_frac": cfg.inactive_frac, "splits": splits, "seed": cfg.seed,
         "page_pool": int(w.cache.shape[0]),
     }
+
+
+def run_config(cfg, w, splits, world) -> dict:
+    """The `config` object of a bench line; both arms print the same one."""
+    kv_bytes, _ = traffic(w, splits)
+    return {**describe(cfg, w, splits),
+            "l2": ("flushed between steps (512 MiB write), per-step CUDA events summed"
+                   if kv_bytes < 4 * L2_BYTES else "inputs larger than L2 (selected K|V per step >> 129 MB)"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
 
 
 def visible_tokens(w) -> np.ndarray:
@@ -379,6 +391,15 @@ def run_reference(args, world, rank):
         return
     cfg = workload_config(args)
     w = inputs.make_workload(cfg, "cpu" if not torch.cuda.is_available() else "cuda:0")
+    # the GPU arm's split count (the page's policy, or the forced one), for the same config record
+    if args.splits:
+        splits = args.splits
+    elif w.window:
+        splits = oracle.sparse_decode_splits(w.rows)
+        while splits > 1 and w.window // splits < 256:
+            splits //= 2
+    else:
+        splits = oracle.sparse_decode_splits(w.rows)
     steps = args.steps or 3
     n_rows = args.cpu_rows or min(w.rows, 48)
     samples = []
@@ -397,7 +418,7 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": describe(cfg, w, 1),
+        "data": "synthetic", "config": run_config(cfg, w, splits, world),
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{n_rows} seeded rows per step of the same workload"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -430,6 +451,7 @@ def run_select(args, dev, world, rank):
             import torch.distributed as dist
             dist.barrier()
         torch.cuda.synchronize()
+        head_start(stream)
         for k in range(steps):
             if flush:
                 scratch.zero_()
@@ -610,6 +632,7 @@ def run_index(args, dev, world, rank, kind):
             dist.barrier()
         torch.cuda.synchronize()
         t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        head_start(stream)
         t_start.record(stream)
         for k in range(steps):
             ev[k][0].record(stream)
@@ -755,19 +778,40 @@ def main():
         return
     cfg = workload_config(args)
     w = inputs.make_workload(cfg, dev)
-    splits = args.splits or (sda.sparse_decode_swa_splits(w.rows, w.window) if w.window
-                             else sda.sparse_decode_splits(w.rows))
-    ws = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8, device=dev)
-    ks = vs = None
-    if w.fp8:
-        ks = torch.tensor([w.k_scale], dtype=torch.float32, device=dev)
-        vs = torch.tensor([w.v_scale], dtype=torch.float32, device=dev)
-    out = torch.empty_like(w.query)
-    kv_bytes, alg_bytes = traffic(w, splits)
-    flush = kv_bytes < 4 * L2_BYTES
-    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
-    stream = torch.cuda.current_stream(dev)
+    splits = args.splits or policy_splits(sda, w)
+    line = run_sparse(args, sda, cfg, w, splits, dev, world, rank)
+    if (world == 1 and not args.no_extra and args.config == "large" and not (args.requests or args.ctx
+                                                                            or args.splits)):
+        # the split + combine path on the same workload, then the small decode workloads
+        # (secondary timings: at least 100 calls each, whatever --steps says)
+        n_extra = max(100, args.steps or 200)
+        line["split_sweep"] = {str(s): time_workload(sda, w, s, dev, args.warmup, n_extra) for s in (2, 4)}
+        del w
+        gc.collect()
+        torch.cuda.empty_cache()
+        extra = {}
+        for name in ("fp8", "gqa"):
+            ew = inputs.make_workload(name, dev)
+            rec = time_workload(sda, ew, policy_splits(sda, ew), dev, args.warmup, n_extra)
+            rec["config"] = run_config(ew.config, ew, rec["splits"], world)
+            extra[name] = rec
+            del ew
+            gc.collect()
+            torch.cuda.empty_cache()
+        line["extra_configs"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
+
+def policy_splits(sda, w) -> int:
+    return sda.sparse_decode_swa_splits(w.rows, w.window) if w.window else sda.sparse_decode_splits(w.rows)
+
+
+def make_step(sda, w, splits, ws, out, stream, ks, vs):
+    """One call of the path on workload w; per-step inputs may be swapped in (e2e)."""
     def step(q=w.query, reg=w.regions, bt=w.block_table, pos=w.positions, act=w.active, gate=w.gate, o=out,
              seq=w.seq_lens, s=None):
         if w.window:
@@ -779,6 +823,79 @@ def main():
                                         query_len=w.query_len, splits=splits, k_scale=ks, v_scale=vs,
                                         gate=gate, region_tokens=w.region_tokens, workspace=ws,
                                         stream=s or stream)
+    return step
+
+
+def device_scales(w, dev):
+    if not w.fp8:
+        return None, None
+    return (torch.tensor([w.k_scale], dtype=torch.float32, device=dev),
+            torch.tensor([w.v_scale], dtype=torch.float32, device=dev))
+
+
+def head_start(stream):
+    """Keeps the GPU busy for ~2 ms (a spin kernel, before any timing event) so that
+    the host queues the first timed calls ahead of the device: an idle stream
+    would otherwise put host-side delays between a start event and its call."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(4_000_000)
+
+
+def timed_calls(step, steps, stream, scratch=None):
+    """Per-call device times (ms) of `steps` calls, each bracketed by CUDA events on
+    the launching stream; with `scratch`, L2 is flushed before each call."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        if scratch is not None:
+            scratch.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_workload(sda, w, splits, dev, warmup, steps) -> dict:
+    """A secondary timing of workload w at `splits` splits: per-call CUDA events,
+    L2 flushed between calls when the selected K|V is not far larger than L2."""
+    ws = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8, device=dev)
+    ks, vs = device_scales(w, dev)
+    out = torch.empty_like(w.query)
+    stream = torch.cuda.current_stream(dev)
+    step = make_step(sda, w, splits, ws, out, stream, ks, vs)
+    kv_bytes, alg_bytes = traffic(w, splits)
+    flush = kv_bytes < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clocks:
+        head_start(stream)
+        per = timed_calls(step, steps, stream, scratch)
+    ms = statistics.mean(per)
+    q = statistics.quantiles(per, n=10) if len(per) > 1 else [per[0]] * 9
+    peak, peak_kind = measured_peak()
+    achieved = alg_bytes / (ms / 1e3) / 1e9
+    return {"rows": w.rows, "splits": splits, "steps": steps, "ms_per_call": ms,
+            "median_ms": statistics.median(per), "p10_ms": q[0], "p90_ms": q[-1], "max_ms": max(per),
+            "rows_per_s": w.rows / (ms / 1e3),
+            "selected_kv_gbs": kv_bytes / (ms / 1e3) / 1e9, "algorithmic_bytes_per_call": alg_bytes,
+            "achieved_gbs": achieved, "frac": achieved / peak, "peak": peak, "peak_kind": peak_kind,
+            "kernels": "sda_split_kernel" + (" + sda_combine_kernel" if splits > 1 else ""),
+            "l2": "flushed between calls" if flush else "inputs larger than L2",
+            "device_flags": sda.read_errors(ws), "clocks": clocks.summary()}
+
+
+def run_sparse(args, sda, cfg, w, splits, dev, world, rank) -> dict:
+    """The headline measurement on one sparse (or window) workload: the bench line."""
+    ws = torch.zeros(sda.workspace_bytes(w.rows, w.heads, splits), dtype=torch.uint8, device=dev)
+    ks, vs = device_scales(w, dev)
+    out = torch.empty_like(w.query)
+    kv_bytes, alg_bytes = traffic(w, splits)
+    flush = kv_bytes < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    stream = torch.cuda.current_stream(dev)
+    step = make_step(sda, w, splits, ws, out, stream, ks, vs)
 
     steps = args.steps or (2000 if not flush else 400)
     for _ in range(args.warmup):
@@ -791,23 +908,17 @@ def main():
             dist.barrier()
 
     # ---- timed region: exactly `steps` calls
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     with ClockSampler(dev) as clocks:
         barrier()
         torch.cuda.synchronize()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
+        head_start(stream)
         t_start.record(stream)
-        for k in range(steps):
-            if flush:
-                scratch.zero_()
-            ev[k][0].record(stream)
-            step()
-            ev[k][1].record(stream)
+        per_launch = timed_calls(step, steps, stream, scratch)          # ms, split (+ combine)
         t_end.record(stream)
         torch.cuda.synchronize()
         barrier()
-    per_launch = [a.elapsed_time(b) for a, b in ev]                 # ms, split (+ combine)
     kernel_ms = sum(per_launch)
     region_ms = t_start.elapsed_time(t_end)
     timed_ms = kernel_ms if flush else region_ms
@@ -825,11 +936,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16" if w.fp8 else "bf16", "data": "synthetic",
-        "config": {**describe(cfg, w, splits),
-                   "l2": ("flushed between steps (512 MiB write), per-step CUDA events summed" if flush
-                          else "inputs larger than L2 (selected K|V per step >> 129 MB)"),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "vs_baseline": None, "dtype": "f16" if w.fp8 else "bf16",
+        "storage_dtype": "fp8_e4m3 cache (decoded exactly to f16 for the MMAs)" if w.fp8 else "bf16",
+        "data": "synthetic",
+        "config": run_config(cfg, w, splits, world),
         "selected_kv_gbs": kv_gbs,
         "unique_kv_gbs": unique_kv_bytes(w) * steps * world / (timed_ms / 1e3) / 1e9,
         "selected_kv_frac_of_peak": kv_gbs / world / peak,
@@ -918,11 +1028,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu:
         n = args.cpu_rows or min(w.rows, 192)
         line["cpu_baseline"] = cpu_baseline(w, n)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    return line
 
 
 if __name__ == "__main__":

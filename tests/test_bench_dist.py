@@ -59,6 +59,10 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "rows/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # the same config record as the GPU arm: the policy's split count (4 rows -> 32), L2 handling
+    # and parallelism included
+    assert d["config"]["splits"] == 32 and d["config"]["parallelism"] == "replicas"
+    assert d["config"]["l2"].startswith("flushed")
 
 
 def test_reference_arm_index_config_under_torchrun():
