@@ -1223,6 +1223,12 @@ sda_status launch(const CUtensorMap &tmap, const Params &prm, int num_regions, c
 
 }  // namespace
 
+// Read by the other translation units' kernels (hidden from the library's exports).
+__attribute__((visibility("hidden"))) uint64_t sda_wait_limit_ns()
+{
+    return g_wait_ns.load();
+}
+
 extern "C" {
 
 int sparse_decode_splits(int rows)

@@ -82,6 +82,13 @@ CASES = {
     "g2_ql1_ragged": dict(requests=7, groups=2, query_len=1, ctx=(511 * 8, 513 * 8 + 7), block=64),
     "g3_ql2": dict(requests=3, groups=3, query_len=2, ctx=(700, 6000), block=32),
     "g6_ql1": dict(requests=3, groups=6, query_len=1, ctx=(3000, 9000), block=64),
+    # pages of 64 tokens or more take the tensor-core variant (128-region tiles)
+    "tc_block128_g2_ql2": dict(requests=3, groups=2, query_len=2, ctx=(5000, 20000), block=128),
+    "tc_block2048_g1_ql3": dict(requests=2, groups=1, query_len=3, ctx=(9000, 40000), block=2048),
+    "tc_block64_g4_ql4": dict(requests=3, groups=4, query_len=4, ctx=(20000, 40000), block=64),
+    "tc_block64_g1_ql3_short": dict(requests=5, groups=1, query_len=3, ctx=(1, 200), block=64),
+    "tc_block64_g2_ql1_capped": dict(requests=3, groups=2, query_len=1, ctx=(3000, 30000), block=64,
+                                     n_cols=2500),
 }
 
 
@@ -123,6 +130,45 @@ def test_bad_page_flags_and_scores_minus_inf():
     ws.zero_()
     run_gpu(w, workspace=ws)
     assert sda.read_errors(ws) == 0
+
+
+def test_bad_page_tensor_core_path():
+    """A page id past the summaries on the 128-region-tile path (64-token pages): flagged, and
+    exactly that page's regions score -inf."""
+    w = inputs.make_index_workload(DEV, requests=3, groups=2, query_len=2, ctx=(6000, 9000), block=64, seed=19)
+    h = host(w)
+    ref = run_oracle(h)
+    scale = run_oracle(h, absolute=True)[0]
+    bad = w.block_table.clone()
+    bad[2, 5] = w.summaries.shape[0]                # past the last page (8 slots per page)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    got = run_gpu(w, table=bad, workspace=ws)
+    assert sda.read_errors(ws) & sda.FLAG_BOUNDS
+    rows = list(range(2 * 2 * 2, 3 * 2 * 2))        # request 2's rows (query_len 2, G = 2)
+    cols = slice(5 * 8, 6 * 8)                      # column 5 of 64-token pages = regions 40..47
+    assert np.all(got[0][rows, cols] == -np.inf)
+    keep = np.ones_like(ref[0], dtype=bool)
+    keep[rows, cols] = False
+    gs = np.where(keep, got[0], ref[0])
+    check((gs, got[1], got[2]), ref, scale)
+
+
+def test_wait_timeout_is_flagged_and_recoverable():
+    """The tensor-core path's pipeline waits honour the process-wide limit: at 0 they run
+    out, the kernel flags SDA_FLAG_TIMEOUT, lets its copies and MMAs finish, releases its
+    tensor memory and returns; the next call with the normal limit is correct."""
+    w = inputs.make_index_workload(DEV, requests=4, groups=4, query_len=2, ctx=(20000, 30000), block=64, seed=23)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    sda.set_wait_limit_ns(0)
+    try:
+        run_gpu(w, workspace=ws)
+    finally:
+        sda.set_wait_limit_ns(10 ** 9)
+    assert sda.read_errors(ws, clear=True) & sda.FLAG_TIMEOUT
+    h = host(w)
+    got = run_gpu(w, workspace=ws)
+    assert sda.read_errors(ws) == 0
+    check(got, run_oracle(h), run_oracle(h, absolute=True)[0])
 
 
 def test_no_columns_still_writes_current_and_lengths():
@@ -249,6 +295,19 @@ def test_padded_summary_slots():
     big[:, w.groups * 256:] = 0x7F                              # NaN codes in the padding
     padded = big[:, :w.groups * 256].view(slots, w.groups, 256)
     assert padded.stride(0) == w.groups * 256 + 64
+    h = host(w)
+    w.summaries = padded
+    check(run_gpu(w), run_oracle(h), run_oracle(h, absolute=True)[0])
+
+
+def test_padded_summary_slots_tensor_core_path():
+    """The same padded slot stride on the 128-region-tile path (64-token pages)."""
+    w = inputs.make_index_workload(DEV, requests=3, groups=4, query_len=3, ctx=(9000, 15000), block=64, seed=13)
+    slots = w.summaries.shape[0]
+    big = torch.zeros((slots, w.groups * 256 + 64), dtype=torch.uint8, device=DEV)
+    big[:, :w.groups * 256] = w.summaries.view(torch.uint8).reshape(slots, -1)
+    big[:, w.groups * 256:] = 0x7F                              # NaN codes in the padding
+    padded = big[:, :w.groups * 256].view(slots, w.groups, 256)
     h = host(w)
     w.summaries = padded
     check(run_gpu(w), run_oracle(h), run_oracle(h, absolute=True)[0])
