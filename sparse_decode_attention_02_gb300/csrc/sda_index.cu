@@ -1217,8 +1217,12 @@ sda_status launch_tc(const sda_tensor *query, const sda_tensor *summaries, const
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         return SDA_ERR_CUDA;
-    // every row set has at least one tile: never more CTAs than tiles
-    const int64_t grid = std::min<int64_t>(reqs * tp.gblocks, static_cast<int64_t>(sms) * kTcCtasPerSm);
+    // one CTA per SM, or fewer when there are fewer tiles than that (a row set has
+    // at most ceil(n_cols / regions per tile) tiles); a CTA whose share of the
+    // tiles is empty sets up and returns
+    const int64_t regions = kTcM / 8 / gblock * 8;
+    const int64_t max_tiles = reqs * tp.gblocks * ((ip.n_cols + regions - 1) / regions);
+    const int64_t grid = std::min<int64_t>(max_tiles, static_cast<int64_t>(sms) * kTcCtasPerSm);
     if (grid < 1)
         return SDA_OK;
     using Fn = cudaError_t (*)(const CUtensorMap &, const CUtensorMap &, const IndexTcParams &, int64_t,
