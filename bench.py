@@ -777,19 +777,14 @@ def main():
             dist.destroy_process_group()
         return
     cfg = workload_config(args)
-    w = inputs.make_workload(cfg, dev)
-    splits = args.splits or policy_splits(sda, w)
-    line = run_sparse(args, sda, cfg, w, splits, dev, world, rank)
-    if (world == 1 and not args.no_extra and args.config == "large" and not (args.requests or args.ctx
-                                                                            or args.splits)):
-        # the split + combine path on the same workload, then the small decode workloads
-        # (secondary timings: at least 100 calls each, whatever --steps says)
-        n_extra = max(100, args.steps or 200)
-        line["split_sweep"] = {str(s): time_workload(sda, w, s, dev, args.warmup, n_extra) for s in (2, 4)}
-        del w
-        gc.collect()
-        torch.cuda.empty_cache()
-        extra = {}
+    extras = (world == 1 and not args.no_extra and args.config == "large"
+              and not (args.requests or args.ctx or args.splits))
+    # secondary timings: at least 100 calls each, whatever --steps says
+    n_extra = max(100, args.steps or 200)
+    extra = {}
+    if extras:
+        # the small decode workloads at the policy's split counts, timed before the
+        # headline's page pool (150+ GB) is built, as each runs on its own
         for name in ("fp8", "gqa"):
             ew = inputs.make_workload(name, dev)
             rec = time_workload(sda, ew, policy_splits(sda, ew), dev, args.warmup, n_extra)
@@ -798,6 +793,12 @@ def main():
             del ew
             gc.collect()
             torch.cuda.empty_cache()
+    w = inputs.make_workload(cfg, dev)
+    splits = args.splits or policy_splits(sda, w)
+    line = run_sparse(args, sda, cfg, w, splits, dev, world, rank)
+    if extras:
+        # the split + combine path on the headline workload
+        line["split_sweep"] = {str(s): time_workload(sda, w, s, dev, args.warmup, n_extra) for s in (2, 4)}
         line["extra_configs"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
