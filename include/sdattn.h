@@ -322,6 +322,20 @@ sda_status sparse_decode_attention_no_alloc(const sda_tensor *query, const sda_t
  */
 sda_status sparse_decode_no_alloc_read_errors(uint32_t *flags, int clear, void *stream);
 
+/*
+ * Diagnostic builds only (the library compiled with SDA_TIMELINE): registers a
+ * device buffer of at least 83886080 bytes (10 x 2^20 uint64) into which the
+ * split and combine kernels of later launches write %globaltimer stamps (ns) at
+ * their phase boundaries: split CTA u at entries u * 8 + k (k = 0 start, 1 the
+ * consumers released with the row's live regions, 2 first K|V stage landed, 3
+ * stage loop done, 4 output writes start, 5 done), combine CTA r at entries
+ * 2^23 + r * 2 + k (k = 0 start, 1 past its wait on the split kernel).  NULL
+ * stops the stamps.  Not thread-safe, synchronous.  The regular library returns
+ * SDA_ERR_UNSUPPORTED and does nothing; its kernels carry no stamps.  No
+ * counterpart on the pages: it is a measurement aid.
+ */
+sda_status sparse_decode_timeline_buffer(void *buffer, size_t bytes);
+
 /* A static description of a status code. */
 const char *sparse_decode_status_string(int status);
 

@@ -23,5 +23,7 @@ from ._binding import (  # noqa: F401
     sparse_decode_swa_attention,
     sparse_decode_swa_splits,
     status_string,
+    timeline_buffer,
+    use_library,
     workspace_bytes,
 )

@@ -80,6 +80,8 @@ def _declare(lib):
     lib.sparse_decode_no_alloc_read_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int,
                                                        ctypes.c_void_p]
     lib.sparse_decode_no_alloc_read_errors.restype = ctypes.c_int
+    lib.sparse_decode_timeline_buffer.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    lib.sparse_decode_timeline_buffer.restype = ctypes.c_int
     lib.sparse_decode_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
     lib.sparse_decode_set_wait_limit_ns.restype = None
     lib.sparse_decode_status_string.argtypes = [ctypes.c_int]
@@ -98,6 +100,16 @@ def load(path: str | None = None):
                 raise ImportError(f"{LIB_PATH} is missing: build it with "
                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
             _lib = _declare(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def use_library(path: str):
+    """Makes every later call of this module go to the library at `path` (a
+    diagnostic build of the same sources, e.g. one compiled with SDA_TIMELINE);
+    returns it."""
+    global _lib
+    with _lock:
+        _lib = _declare(ctypes.CDLL(path))
     return _lib
 
 
@@ -379,3 +391,14 @@ def no_alloc_read_errors(clear: bool = False, stream: torch.cuda.Stream | None =
     if rc != SDA_OK:
         raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())
     return out.value
+
+
+def timeline_buffer(buffer: torch.Tensor | None) -> None:
+    """Registers a device buffer for the kernels' phase stamps (a library built
+    with SDA_TIMELINE only; the regular one raises SdaError UNSUPPORTED)."""
+    lib = load()
+    ptr = buffer.data_ptr() if buffer is not None else None
+    nbytes = buffer.numel() * buffer.element_size() if buffer is not None else 0
+    rc = lib.sparse_decode_timeline_buffer(ptr, nbytes)
+    if rc != SDA_OK:
+        raise SdaError(rc, lib.sparse_decode_status_string(rc).decode())

@@ -55,6 +55,32 @@ constexpr float kRescaleSlack = 8.0f;      // log2 units a running max may lag t
 constexpr size_t kHeaderBytes = 256;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
+// Diagnostic builds (compiled with SDA_TIMELINE) stamp %globaltimer at phase
+// boundaries into a device buffer registered with sparse_decode_timeline_buffer:
+// split CTA u writes entries u * 8 + k (k = 0 entry, 1 consumers released, 2
+// first stage seen, 3 stage loop done, 4 output writes start, 5 done), combine
+// CTA r entries kTimelineCombine + r * 2 + k (k = 0 entry, 1 past the wait on
+// the split kernel).  The regular build compiles every stamp away.
+constexpr unsigned long long kTimelineUnits = 1ull << 20;
+constexpr unsigned long long kTimelineCombine = 8 * kTimelineUnits;
+constexpr size_t kTimelineBytes = (8 + 2) * kTimelineUnits * sizeof(unsigned long long);
+#ifdef SDA_TIMELINE
+__device__ unsigned long long *g_sda_timeline = nullptr;
+#define SDA_STAMP(cond, idx)                                                                       \
+    do {                                                                                           \
+        unsigned long long *tl_ = g_sda_timeline;                                                  \
+        if ((cond) && tl_) {                                                                       \
+            unsigned long long t_;                                                                 \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                  \
+            tl_[idx] = t_;                                                                         \
+        }                                                                                          \
+    } while (0)
+#else
+#define SDA_STAMP(cond, idx) \
+    do {                     \
+    } while (0)
+#endif
+
 
 template <bool FP8>
 struct Traits;
@@ -470,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     pdl_launch_dependents();
     pdl_wait();   // inputs may be written by the previous kernel on the stream
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 0);
 
     // Sparse mode: the row's selected regions, its position and active flag.
     // Window mode: every row is active; token j = (row / G) % query_len of a
@@ -552,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // Release the consumers (barriers, stage count) without waiting for
         // their Q fragments: the producer starts streaming right away.
         asm volatile("bar.arrive 2, %0;" ::"n"(kThreads) : "memory");
+        SDA_STAMP(lane == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 1);
     } else {
         // ---- Consumers: Q A-fragments into shared memory, in fragment order
         // ([k-step][lane] x 4 words).  K-step kk of thread t covers the four
@@ -810,6 +838,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int s = st % T::kStages;
         const uint32_t par = static_cast<uint32_t>(st / T::kStages) & 1u;
         const bool ok = mbar_wait(full_bar + 8 * s, par, p.wait_ns);
+        SDA_STAMP(st == pair && warp == 0 && lane == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 2);
         if (!__all_sync(~0u, ok)) {
             if (lane == 0)
                 atomicOr(p.flags, SDA_FLAG_TIMEOUT);
@@ -950,6 +979,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_arrive(empty_bar + 8 * s);
     }
 
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 3);
     // ---- Epilogue: merge the four warps.
     float l0 = l_run[0], l1 = l_run[1];
     l0 += __shfl_xor_sync(~0u, l0, 1);
@@ -1030,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     consumer_bar();
 
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 4);
     const int total = p.heads * kDim;
     if constexpr (PAIR) {                  // token k's rows: warps 2k and 2k + 1
         for (int e = ctid; e < 2 * total; e += kConsumerWarps * 32) {
@@ -1071,6 +1102,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             dst[e] = v * vfold;
         }
     }
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, blockIdx.x * 8ull + 5);
 }
 
 // ---------------------------------------------------------------------------
@@ -1083,7 +1115,9 @@ constexpr int kCombineThreads = kMaxHeads * (kDim / 4);   // 768
 
 __global__ void __launch_bounds__(kCombineThreads) sda_combine_kernel(const __grid_constant__ Params p)
 {
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, kTimelineCombine + blockIdx.x * 2ull);
     pdl_wait();   // partials come from the split kernel
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, kTimelineCombine + blockIdx.x * 2ull + 1);
     const int row = blockIdx.x;
     const int item = threadIdx.x;
     if (item >= p.heads * (kDim / 4))
@@ -1269,6 +1303,20 @@ const char *sparse_decode_status_string(int status)
     case SDA_ERR_BOUNDS: return "an index read from the inputs was out of range";
     default: return "unknown status";
     }
+}
+
+sda_status sparse_decode_timeline_buffer(void *buffer, size_t bytes)
+{
+#ifdef SDA_TIMELINE
+    if (buffer && bytes < kTimelineBytes)
+        return SDA_ERR_INVALID;
+    unsigned long long *ptr = static_cast<unsigned long long *>(buffer);
+    return cudaMemcpyToSymbol(g_sda_timeline, &ptr, sizeof ptr) == cudaSuccess ? SDA_OK : SDA_ERR_CUDA;
+#else
+    (void)buffer;
+    (void)bytes;
+    return SDA_ERR_UNSUPPORTED;
+#endif
 }
 
 sda_status sparse_decode_read_errors(const void *workspace, uint32_t *flags, int clear, void *stream)

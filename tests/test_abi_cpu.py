@@ -295,3 +295,13 @@ def test_swa_splits_policy(lib):
                 while want > 1 and window // want < 256:
                     want //= 2
                 assert sda.sparse_decode_swa_splits(rows, window) == want, (rows, window)
+
+
+def test_timeline_entry_point_is_a_stub_in_the_regular_library():
+    """The phase stamps exist only in a diagnostic build (SDA_TIMELINE); the regular
+    library refuses the buffer without touching the GPU."""
+    import ctypes
+    from sparse_decode_attention_02_gb300 import _binding as B
+    lib = B.load()
+    assert lib.sparse_decode_timeline_buffer(None, 0) == B.SDA_ERR_UNSUPPORTED
+    assert lib.sparse_decode_timeline_buffer(ctypes.c_void_p(16), 1 << 30) == B.SDA_ERR_UNSUPPORTED
