@@ -78,7 +78,7 @@ def test_random_window_shapes(seed):
 
 def index_case(seed):
     rng = np.random.default_rng(3000 + seed)
-    block = int(rng.choice([8, 16, 32, 64, 128]))
+    block = int(rng.choice([8, 16, 32, 64, 128, 256]))   # 64 and up: the tensor-core kernel
     lo = int(rng.integers(1, 3000))
     kw = dict(requests=int(rng.integers(1, 6)), groups=int(rng.integers(1, 9)),
               query_len=int(rng.integers(1, 5)), ctx=(lo, lo + int(rng.integers(0, 9000))), block=block,
@@ -88,7 +88,7 @@ def index_case(seed):
     return kw
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(24))
 def test_random_indexer_shapes(seed):
     import torch
     import oracle

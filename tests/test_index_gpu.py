@@ -89,6 +89,10 @@ CASES = {
     "tc_block64_g1_ql3_short": dict(requests=5, groups=1, query_len=3, ctx=(1, 200), block=64),
     "tc_block64_g2_ql1_capped": dict(requests=3, groups=2, query_len=1, ctx=(3000, 30000), block=64,
                                      n_cols=2500),
+    # one group per block (N = 16 with 8 padding rows at query_len 1, 32 with 8 at query_len 3)
+    "tc_block64_g3_ql1": dict(requests=4, groups=3, query_len=1, ctx=(2000, 12000), block=64),
+    "tc_block64_g5_ql3": dict(requests=3, groups=5, query_len=3, ctx=(500, 9000), block=64),
+    "tc_block256_g2_ql4_short": dict(requests=6, groups=2, query_len=4, ctx=(1, 2100), block=256),
 }
 
 
