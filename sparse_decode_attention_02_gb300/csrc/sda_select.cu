@@ -11,13 +11,15 @@
 //
 // One CTA of 256 threads per row (4 per SM), scores compared as
 // order-preserving 32-bit keys; the row is prefetched into L2 at entry.
-//   Fast path (rows of up to 64K candidates): a low threshold is estimated
-//   from a 2048-score sample so that the topk best scores pass it with a
+//   Fast path (rows of up to 64K candidates): a 16-bit lower bound is read
+//   off a 2048-score sample so that the topk best scores pass it with a
 //   margin of five binomial standard deviations; one streaming pass (a plain
-//   float comparison against the threshold's smallest passing value) keeps
-//   the passing (key, id) pairs in shared memory; an exact radix select on
-//   that buffer gives the last kept key; bitmaps over the ids give the
-//   lowest-id ties and the ascending output.
+//   float comparison against the bound's smallest passing value, one warp
+//   ballot per 32 ids) writes a bitmap of the passing ids; their keys are
+//   gathered (L2 hits) into a shared buffer in ascending id order while a
+//   histogram of their 16-bit prefixes is built; the prefix holding rank topk
+//   and a one-warp ranking of its few keys give the exact last kept key; one
+//   block scan over the buffer places the kept ids and the lowest-id ties.
 //   Fallback (buffer overflow or underflow, longer rows): an exact 4-pass
 //   radix select that streams the row each pass, then an ordered compaction.
 #include <cuda_runtime.h>
@@ -34,9 +36,9 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kSelBatch = 8;                     // loads in flight per thread (exact passes)
 constexpr int kFilterBatch = 16;                 // loads in flight per thread (filter pass)
 constexpr int kFilterStep = kSelThreads * kFilterBatch;
+constexpr int kGather = 8;                      // candidate key loads in flight per thread
 constexpr int kSample = 2048;                    // scores sampled for the filter threshold
-constexpr int kBufCap = 4080;                    // filtered (key, id) pairs held in shared memory
-                                                 // (57,260 bytes in all: 4 CTAs per SM)
+constexpr int kBufCap = 4080;                    // candidate (key, id) pairs held in shared memory
 constexpr int kFastMaxLen = 65536;               // longest row the bitmaps cover
 constexpr int kBitWords = kFastMaxLen / 32;
 
@@ -55,13 +57,13 @@ struct SelectParams {
 struct SelShared {
     uint32_t whist[kSelWarps][256];              // per-warp histograms; row 0 then holds the sums
     uint32_t cnt[kSelWarps];
-    uint32_t found[2];                           // digit, keys above it
-    uint32_t counter;
+    uint32_t found[3];                           // digit (or prefix), keys above it, keys in it
+    uint32_t counter;                            // fill of bin_keys
     union {
         uint32_t sample[kSample];
         struct {
-            uint32_t kept[kBitWords];
-            uint32_t tie[kBitWords];
+            uint32_t kept[kBitWords];            // candidate bitmap of the streaming pass
+            uint32_t bin_keys[32];               // keys sharing the 16-bit prefix of rank topk
         } bits;
     } a;
     uint32_t buf_key[kBufCap];
@@ -69,6 +71,12 @@ struct SelShared {
 };
 // 4 CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
 static_assert(sizeof(SelShared) <= 4 * 1024 * 14, "selection shared memory above 4 CTAs per SM");
+// The streaming pass stores one bitmap word per lane below kFilterBatch and
+// never past the bitmap; the prefix histogram is the 2048 words of whist, 8
+// bins per thread; the sample is 8 scores per thread.
+static_assert(kFilterBatch <= 32 && kFastMaxLen % kFilterStep == 0, "streaming pass layout");
+static_assert(kSelWarps * 256 == 2048 && 8 * kSelThreads == 2048, "prefix histogram layout");
+static_assert(kSample % kSelThreads == 0, "sample layout");
 
 // Order-preserving key: a larger score gives a larger key; NaN is the
 // smallest key and -0 equals +0.
@@ -189,20 +197,23 @@ __device__ __forceinline__ void find_digit(SelShared &sh, int remaining)
 // Key of descending rank `rank` (1 <= rank <= n) among keys[0, n) in shared
 // memory; *above gets the number of keys strictly greater.  With `digits` < 4
 // only the top 8 * digits bits are resolved and the lower bits are zero: a
-// lower bound of that key.
+// lower bound of that key.  With `first_ready` the caller has already built
+// the per-warp histograms of the top digit (key >> 24) over all n keys.
 __device__ uint32_t select_shared(SelShared &sh, const uint32_t *keys, int n, int rank, int *above,
-                                  int digits = 4)
+                                  int digits = 4, bool first_ready = false)
 {
     const int warp = threadIdx.x >> 5;
     uint32_t prefix = 0, mask = 0;
     int remaining = rank;
     for (int shift = 24; shift >= 32 - 8 * digits; shift -= 8) {
-        zero_whist(sh);
-        __syncthreads();
-        for (int i = threadIdx.x; i < n; i += kSelThreads) {
-            const uint32_t key = keys[i];
-            if ((key & mask) == prefix)
-                atomicAdd(&sh.whist[warp][(key >> shift) & 255u], 1u);
+        if (!(first_ready && shift == 24)) {
+            zero_whist(sh);
+            __syncthreads();
+            for (int i = threadIdx.x; i < n; i += kSelThreads) {
+                const uint32_t key = keys[i];
+                if ((key & mask) == prefix)
+                    atomicAdd(&sh.whist[warp][(key >> shift) & 255u], 1u);
+            }
         }
         find_digit(sh, remaining);
         remaining -= static_cast<int>(sh.found[1]);
@@ -283,9 +294,14 @@ __global__ void __launch_bounds__(kSelThreads, 4) sda_select_kernel(const __grid
         // ---- filter threshold from a sample (all candidates when few)
         uint32_t t_lo = 0u;
         if (cand > kBufCap) {
-            for (int j = tid; j < kSample; j += kSelThreads)
-                sh.a.sample[j] = score_key(sc[static_cast<int64_t>(j) * len / kSample]);
+            // the first radix digit's histogram is built as the sample loads
+            zero_whist(sh);
             __syncthreads();
+            for (int j = tid; j < kSample; j += kSelThreads) {
+                const uint32_t key = score_key(sc[static_cast<int64_t>(j) * len / kSample]);
+                sh.a.sample[j] = key;
+                atomicAdd(&sh.whist[tid >> 5][key >> 24], 1u);
+            }
             // Sample rank of the bound: the sample's expected count of the row's
             // top k (a binomial mean mu) plus five standard deviations and a
             // constant, so that fewer than k candidates reach the bound only
@@ -293,32 +309,32 @@ __global__ void __launch_bounds__(kSelThreads, 4) sda_select_kernel(const __grid
             const float mu = static_cast<float>(k) * kSample / static_cast<float>(cand);
             const int r = min(kSample, static_cast<int>(mu + 5.0f * sqrtf(mu)) + 17);
             int unused;
-            t_lo = select_shared(sh, sh.a.sample, kSample, r, &unused, 2);   // 16-bit lower bound
+            t_lo = select_shared(sh, sh.a.sample, kSample, r, &unused, 2, true);   // 16-bit lower bound
         }
-        // ---- one streaming pass: (key, id) pairs with key >= t_lo
-        if (tid == 0)
-            sh.counter = 0;
-        __syncthreads();
-        // Each thread marks its kept scores in a bit mask; one warp scan and one
-        // shared counter update per batch place them.  With t_lo > 0 the test
-        // key >= t_lo is the float comparison x >= key_floor_value(t_lo), so a
-        // key is formed only for a kept score; batches wholly inside the row and
-        // clear of the current region skip the per-score id checks.
+        // ---- one streaming pass: a bitmap of the candidates with key >= t_lo.
+        // Element e of a batch is id b0 + 256 e + tid, so for each e a warp's
+        // lanes hold 32 consecutive ids: one ballot forms that bitmap word, and
+        // lane e stores it.  With t_lo > 0 the test key >= t_lo is the float
+        // comparison x >= key_floor_value(t_lo); batches wholly inside the row
+        // and clear of the current region skip the per-score id checks.
         const int excl = forced ? cur : -1;
         const bool keep_all = t_lo == 0u;
         const float x_lo = keep_all ? 0.0f : key_floor_value(t_lo);
+        const int warp = tid >> 5;
         for (int b0 = 0; b0 < len; b0 += kFilterStep) {
             const bool plain = !keep_all && b0 + kFilterStep <= len && (excl < b0 || excl >= b0 + kFilterStep);
             float v[kFilterBatch];
-            uint32_t keepm = 0;
+            uint32_t mine = 0;
             if (plain) {
                 const float *src = sc + b0 + tid;
 #pragma unroll
                 for (int e = 0; e < kFilterBatch; ++e)
                     v[e] = src[e * kSelThreads];
 #pragma unroll
-                for (int e = 0; e < kFilterBatch; ++e)
-                    keepm |= static_cast<uint32_t>(v[e] >= x_lo) << e;
+                for (int e = 0; e < kFilterBatch; ++e) {
+                    const uint32_t w = __ballot_sync(~0u, v[e] >= x_lo);
+                    mine = lane == e ? w : mine;
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < kFilterBatch; ++e) {
@@ -328,86 +344,151 @@ __global__ void __launch_bounds__(kSelThreads, 4) sda_select_kernel(const __grid
 #pragma unroll
                 for (int e = 0; e < kFilterBatch; ++e) {
                     const int i = b0 + e * kSelThreads + tid;
-                    keepm |= static_cast<uint32_t>(i < len && i != excl && (keep_all || v[e] >= x_lo)) << e;
+                    const uint32_t w = __ballot_sync(~0u, i < len && i != excl && (keep_all || v[e] >= x_lo));
+                    mine = lane == e ? w : mine;
                 }
             }
-            const int cnt = __popc(keepm);
-            int incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int x = __shfl_up_sync(~0u, incl, o);
-                if (lane >= o)
-                    incl += x;
-            }
-            uint32_t wbase = 0;
-            if (lane == 31 && incl)
-                wbase = atomicAdd(&sh.counter, static_cast<uint32_t>(incl));
-            uint32_t at = __shfl_sync(~0u, wbase, 31) + static_cast<uint32_t>(incl - cnt);
-            if (keepm) {
-#pragma unroll
-                for (int e = 0; e < kFilterBatch; ++e) {
-                    if ((keepm >> e) & 1u) {
-                        if (at < static_cast<uint32_t>(kBufCap)) {
-                            sh.buf_key[at] = score_key(v[e]);
-                            sh.buf_id[at] = b0 + e * kSelThreads + tid;
-                        }
-                        ++at;
+            if (lane < kFilterBatch)   // word of ids b0 + 256 lane + 32 warp + [0, 32)
+                sh.a.bits.kept[(b0 >> 5) + lane * kSelWarps + warp] = mine;
+        }
+        __syncthreads();
+        // ---- the candidates' ids into the buffer, ascending: thread t owns
+        // bitmap words [t W, t W + W)
+        const int words = (len + 31) / 32;
+        const int W = (words + kSelThreads - 1) / kSelThreads;
+        const int w0 = tid * W, w1 = min(words, w0 + W);
+        int total;
+        {
+            int c = 0;
+            for (int w = w0; w < w1; ++w)
+                c += __popc(sh.a.bits.kept[w]);
+            int at = block_excl_sum(c, sh.cnt, &total);
+            if (total <= kBufCap && total >= k) {
+                for (int w = w0; w < w1; ++w) {   // candidate ids, ascending
+                    uint32_t b = sh.a.bits.kept[w];
+                    while (b) {
+                        const int bit = __ffs(b) - 1;
+                        b &= b - 1;
+                        sh.buf_id[at++] = w * 32 + bit;
                     }
                 }
             }
         }
-        __syncthreads();
-        const int total = static_cast<int>(sh.counter);
+        uint32_t *const hist = &sh.whist[0][0];   // 2048 bins: 16-bit key prefixes above t_lo's
+        const uint32_t hi0 = t_lo >> 16;
         if (total <= kBufCap && total >= k) {
-            // ---- exact select inside the buffer
-            int above;
-            thr = select_shared(sh, sh.buf_key, total, k, &above);
+            if (t_lo != 0u)
+                for (int b = tid; b < kSelWarps * 256; b += kSelThreads)
+                    hist[b] = 0;
+            if (tid == 0)
+                sh.counter = 0;
+            __syncthreads();
+            // their keys (the row has just streamed through, so these loads hit L2)
+            // and, over a 16-bit bound, the histogram of their prefixes
+            for (int i0 = 0; i0 < total; i0 += kSelThreads * kGather) {
+                float g[kGather];
+#pragma unroll
+                for (int e = 0; e < kGather; ++e) {
+                    const int i = i0 + e * kSelThreads + tid;
+                    g[e] = i < total ? sc[sh.buf_id[i]] : 0.0f;
+                }
+#pragma unroll
+                for (int e = 0; e < kGather; ++e) {
+                    const int i = i0 + e * kSelThreads + tid;
+                    if (i < total) {
+                        const uint32_t key = score_key(g[e]);
+                        sh.buf_key[i] = key;
+                        if (t_lo != 0u)
+                            atomicAdd(&hist[min((key >> 16) - hi0, 2047u)], 1u);
+                    }
+                }
+            }
+            // ---- exact select inside the buffer: the key of descending rank k
+            int above = 0;
+            bool found = false;
+            if (t_lo != 0u) {
+                // the prefix holding rank k: thread t owns prefixes [8 (255 - t), 8 (255 - t) + 8)
+                __syncthreads();
+                const int hb = 8 * (kSelThreads - 1 - tid);
+                uint32_t hc[8];
+                int s8 = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    hc[j] = hist[hb + 7 - j];
+                    s8 += static_cast<int>(hc[j]);
+                }
+                int all;
+                const int before = block_excl_sum(s8, sh.cnt, &all);
+                if (before < k && k <= before + s8) {
+                    int acc = before;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (acc + static_cast<int>(hc[j]) >= k) {
+                            sh.found[0] = static_cast<uint32_t>(hb + 7 - j);
+                            sh.found[1] = static_cast<uint32_t>(acc);
+                            sh.found[2] = hc[j];
+                            break;
+                        }
+                        acc += static_cast<int>(hc[j]);
+                    }
+                }
+                __syncthreads();
+                // read from the finder's broadcast, not from hist, which the
+                // fallback below zeroes at once: the branch is block-uniform
+                const uint32_t bin = sh.found[0];
+                const int above_bin = static_cast<int>(sh.found[1]);
+                const int in_bin = static_cast<int>(sh.found[2]);
+                if (bin < 2047u && in_bin <= 32) {
+                    // the prefix's keys (at most 32) ranked by one warp
+                    for (int e = tid; e < total; e += kSelThreads) {
+                        const uint32_t key = sh.buf_key[e];
+                        if ((key >> 16) - hi0 == bin)
+                            sh.a.bits.bin_keys[atomicAdd(&sh.counter, 1u)] = key;
+                    }
+                    __syncthreads();
+                    if (tid < 32) {
+                        const uint32_t mine = tid < in_bin ? sh.a.bits.bin_keys[tid] : 0u;
+                        int gt = 0, eq = 0;
+                        for (int j = 0; j < in_bin; ++j) {
+                            const uint32_t o = __shfl_sync(~0u, mine, j);
+                            gt += o > mine;
+                            eq += o == mine;
+                        }
+                        const int need = k - above_bin;
+                        if (tid < in_bin && gt < need && need <= gt + eq) {   // equal keys write equal values
+                            sh.found[0] = mine;
+                            sh.found[1] = static_cast<uint32_t>(above_bin + gt);
+                        }
+                    }
+                    __syncthreads();
+                    thr = sh.found[0];
+                    above = static_cast<int>(sh.found[1]);
+                    found = true;
+                }
+            }
+            if (!found)
+                thr = select_shared(sh, sh.buf_key, total, k, &above);
             take_eq = k - above;
-            const int words = (len + 31) / 32;
-            for (int w = tid; w < words; w += kSelThreads) {
-                sh.a.bits.kept[w] = 0;
-                sh.a.bits.tie[w] = 0;
-            }
-            __syncthreads();
-            for (int e = tid; e < total; e += kSelThreads) {
+            // ---- output: the buffer's ids ascend, so thread t's slice [t C, t C + C)
+            // keeps its keys above thr and its ties while fewer than take_eq precede them
+            const int C = (total + kSelThreads - 1) / kSelThreads;
+            const int e0 = min(total, tid * C), e1 = min(total, e0 + C);
+            int strict = 0, ties = 0;
+            for (int e = e0; e < e1; ++e) {
                 const uint32_t key = sh.buf_key[e];
-                const int id = sh.buf_id[e];
-                if (key > thr)
-                    atomicOr(&sh.a.bits.kept[id >> 5], 1u << (id & 31));
-                else if (key == thr)
-                    atomicOr(&sh.a.bits.tie[id >> 5], 1u << (id & 31));
+                strict += key > thr;
+                ties += key == thr;
             }
-            __syncthreads();
-            // thread t owns words [t * W, t * W + W): ties in id order, then the output
-            const int W = (words + kSelThreads - 1) / kSelThreads;
-            const int w0 = tid * W, w1 = min(words, w0 + W);
-            int ties = 0;
-            for (int w = w0; w < w1; ++w)
-                ties += __popc(sh.a.bits.tie[w]);
-            int tie_total;
-            int rank = block_excl_sum(ties, sh.cnt, &tie_total);
-            int kept = 0;
-            for (int w = w0; w < w1; ++w) {
-                uint32_t tb = sh.a.bits.tie[w];
-                while (tb) {
-                    const int bit = __ffs(tb) - 1;
-                    tb &= tb - 1;
-                    if (rank++ < take_eq)
-                        sh.a.bits.kept[w] |= 1u << bit;
-                }
-                kept += __popc(sh.a.bits.kept[w]);
+            int sums;
+            const int before = block_excl_sum((ties << 16) | strict, sh.cnt, &sums);
+            int tie_rank = before >> 16;
+            int pos = base + (before & 0xFFFF) + min(tie_rank, take_eq);
+            for (int e = e0; e < e1; ++e) {
+                const uint32_t key = sh.buf_key[e];
+                if (key > thr || (key == thr && tie_rank++ < take_eq))
+                    out[pos++] = sh.buf_id[e];
             }
-            int kept_total;
-            int pos = base + block_excl_sum(kept, sh.cnt, &kept_total);
-            for (int w = w0; w < w1; ++w) {
-                uint32_t kb = sh.a.bits.kept[w];
-                while (kb) {
-                    const int bit = __ffs(kb) - 1;
-                    kb &= kb - 1;
-                    out[pos++] = w * 32 + bit;
-                }
-            }
-            written = kept_total;
+            written = (sums & 0xFFFF) + min(sums >> 16, take_eq);
             done = true;
         }
     }

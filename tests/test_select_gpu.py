@@ -111,3 +111,45 @@ def test_select_special_floats(seed):
         got = sda.sparse_decode_select_regions(t(sc), t(cur), topk, topk_lengths=t(lens))
         torch.cuda.synchronize()
         assert np.array_equal(got.cpu().numpy(), oracle.select_regions(sc, cur, topk, lens)), topk
+
+
+def _keys(sc):
+    """Order-preserving 32-bit keys of float32 scores (NaN lowest, -0 == +0)."""
+    u = np.ascontiguousarray(sc, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = np.where((u & 0x7FFFFFFF) == 0, 0, u)
+    k = np.where(u & 0x80000000, ~u & 0xFFFFFFFF, u | 0x80000000)
+    return np.where(np.isnan(sc), 0, k).astype(np.uint64)
+
+
+@pytest.mark.parametrize("case", ["spread", "ties", "wide"])
+def test_select_threshold_in_buffer(case):
+    """Rows long enough for the sampled bound, shaped so that the exact threshold among the
+    buffered candidates is found each way the kernel has: by ranking the few keys that share
+    the 16-bit prefix of rank topk (normal scores), by a radix select when more than 32 keys
+    share it (scores on a 0.5 grid), and when that prefix lies 2047 or more prefixes above
+    the bound's (log-normal scores over ~250 octaves)."""
+    rng = np.random.default_rng({"spread": 11, "ties": 12, "wide": 13}[case])
+    rows, n, topk = 6, 20000, 1024
+    z = rng.standard_normal((rows, n))
+    sc = {"spread": z, "ties": np.round(z * 2) / 2,
+          "wide": np.exp(np.clip(z * 80 - 60, -87, 87))}[case]
+    sc = sc.astype(np.float32)
+    lens = np.full(rows, n, dtype=np.int32)
+    cur = rng.integers(0, n, size=rows).astype(np.int32)
+    for r in range(rows):                      # the branch each row reaches, from the keys alone
+        keys = np.delete(_keys(sc[r]), cur[r])
+        kth = np.sort(keys)[::-1][topk - 2]    # topk - 1 others besides the current region
+        in_prefix = int(np.sum((keys >> 16) == (kth >> 16)))
+        if case == "spread":
+            assert in_prefix <= 32
+        elif case == "ties":
+            assert in_prefix > 32
+        else:
+            samp = np.sort(_keys(sc[r][(np.arange(2048) * n) // 2048]))[::-1]
+            mu = np.float32(topk - 1) * 2048 / np.float32(n - 1)
+            bound = samp[min(2048, int(mu + 5 * np.sqrt(mu)) + 17) - 1] >> 16
+            assert (kth >> 16) - bound >= 2047
+    t = lambda a: torch.as_tensor(a, device=DEV)
+    got = sda.sparse_decode_select_regions(t(sc), t(cur), topk, topk_lengths=t(lens))
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), oracle.select_regions(sc, cur, topk, lens))
