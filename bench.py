@@ -5,8 +5,13 @@ when splits > 1) over one batch of a synthetic workload resident in HBM.
 Default workload: "large" (512 requests x G=4 rows, 16 heads, FP8 E4M3
 cache, R=128 regions of 64 tokens, contexts 128K-256K, 2048 rows).
 
-Prints ONE JSON line (rank 0).  `--impl reference` times the float64 CPU
-oracle on the same workload instead (the reference arm of this benchmark).
+Prints ONE JSON line (rank 0).  On one GPU the default run also times, each
+on its own and before the headline workload is built, forced split counts 2
+and 4 on the headline workload (`split_sweep`) and every other workload
+(`extra_configs`: tiny, gqa, fp8, spec and swa at the policy's split counts,
+region selection, the indexer and the whole decode step); `--no-extra` skips
+them.  `--impl reference` times the float64 CPU oracle on the same workload
+instead (the reference arm of this benchmark).
 Multi-GPU (torchrun): every rank runs an independent replica of the
 workload (rows are independent; no collective on the data path).
 """
@@ -427,7 +432,7 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def run_select(args, dev, world, rank):
+def run_select(args, dev, world, rank, emit=True):
     """Region selection alone: 2048 decode rows (the large workload's rows), ids of
     8-token regions up to each row's position (16K-32K candidates), top-1024."""
     import sparse_decode_attention_02_gb300 as sda
@@ -488,8 +493,9 @@ def run_select(args, dev, world, rank):
         line["cpu_baseline"] = {"value": n * runs / dt, "unit": "rows/s", "cores": oracle.num_threads(),
                                 "kind": "oracle",
                                 "sample": f"first {n} rows, {runs} runs ({dt:.1f} s, full sort per row)"}
-    if rank == 0:
+    if rank == 0 and emit:
         print(json.dumps(line), flush=True)
+    return line
 
 
 INDEX_METRIC = ("indexer score rows/s (8-token region summaries, 16K-32K regions per (token, KV group) "
@@ -582,7 +588,7 @@ def index_kw(args) -> dict:
     return kw
 
 
-def run_index(args, dev, world, rank, kind):
+def run_index(args, dev, world, rank, kind, emit=True):
     """The indexer alone (`index`), or a whole DSA decode step (`decode`):
     indexer scores -> region selection -> sparse attention over 8-token regions."""
     import sparse_decode_attention_02_gb300 as sda
@@ -743,8 +749,9 @@ def run_index(args, dev, world, rank, kind):
         rows, dt, what = cpu_index_sample(args, kind, ch or iw, min_seconds=CPU_MIN_SECONDS)
         line["cpu_baseline"] = {"value": rows / dt, "unit": "rows/s", "cores": oracle.num_threads(),
                                 "kind": "oracle", "sample": f"{what} ({dt:.2f} s, float64 C)"}
-    if rank == 0:
+    if rank == 0 and emit:
         print(json.dumps(line), flush=True)
+    return line
 
 
 def main():
@@ -783,14 +790,25 @@ def main():
     n_extra = max(100, args.steps or 200)
     extra = {}
     if extras:
-        # the small decode workloads at the policy's split counts, timed before the
-        # headline's page pool (150+ GB) is built, as each runs on its own
-        for name in ("fp8", "gqa"):
+        # every other workload, each on its own and freed before the headline's page
+        # pool (150+ GB) is built: the sparse and window decode workloads at the
+        # policy's split counts, then region selection, the indexer and the whole
+        # decode step (indexer -> selection -> attention) through their own runners
+        for name in ("tiny", "gqa", "fp8", "spec", "swa"):
             ew = inputs.make_workload(name, dev)
             rec = time_workload(sda, ew, policy_splits(sda, ew), dev, args.warmup, n_extra)
             rec["config"] = run_config(ew.config, ew, rec["splits"], world)
             extra[name] = rec
             del ew
+            gc.collect()
+            torch.cuda.empty_cache()
+        sub = argparse.Namespace(**{**vars(args), "steps": n_extra, "no_cpu": True, "no_e2e": True})
+        for name, run in (("select", lambda: run_select(sub, dev, world, rank, emit=False)),
+                          ("index", lambda: run_index(sub, dev, world, rank, "index", emit=False)),
+                          ("decode", lambda: run_index(sub, dev, world, rank, "decode", emit=False))):
+            rec = run()
+            extra[name] = {k: rec[k] for k in rec if k not in ("n_gpus", "warmup", "scaling", "vs_baseline",
+                                                                 "data", "higher_is_better")}
             gc.collect()
             torch.cuda.empty_cache()
     w = inputs.make_workload(cfg, dev)
