@@ -315,3 +315,99 @@ def test_padded_summary_slots_tensor_core_path():
     h = host(w)
     w.summaries = padded
     check(run_gpu(w), run_oracle(h), run_oracle(h, absolute=True)[0])
+
+
+def _chain_step(w, cache, query, positions, active, topk, bufs, stream):
+    """One decode step (scores -> selection -> attention) into the tensors of `bufs`."""
+    scores, cur, lens, regions, out, ws = bufs
+    sda.sparse_decode_summary_scores(w.query, w.weights, w.summaries, w.block_table, w.seq_lens,
+                                     block_size=w.block, query_len=w.query_len, scores=scores,
+                                     current=cur, lengths=lens, workspace=ws, stream=stream)
+    sda.sparse_decode_select_regions(scores, cur, topk, regions, topk_lengths=lens, stream=stream)
+    sda.sparse_decode_attention(query, cache, regions, w.block_table, positions, active, out,
+                                scale=192 ** -0.5, query_len=w.query_len, splits=2, region_tokens=8,
+                                workspace=ws, stream=stream)
+
+
+def _chain_inputs(w, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    pages = w.summaries.shape[0] // (w.block // 8)
+    cache = torch.randn((pages, w.groups, w.block, 384), generator=g, device=DEV).to(torch.bfloat16)
+    query = torch.randn((w.rows, 16, 192), generator=g, device=DEV).to(torch.bfloat16)
+    seq = w.seq_lens.long()
+    tok = torch.arange(w.tokens, device=DEV)
+    positions = (seq[tok // w.query_len] - w.query_len + tok % w.query_len).repeat_interleave(w.groups)
+    return cache, query, positions.to(torch.int32), torch.ones(w.rows, dtype=torch.bool, device=DEV)
+
+
+def _chain_bufs(w, topk):
+    return (torch.full((w.rows, w.n_cols), float("nan"), device=DEV),
+            torch.full((w.rows,), -7, dtype=torch.int32, device=DEV),
+            torch.full((w.rows,), -7, dtype=torch.int32, device=DEV),
+            torch.full((w.rows, topk), -7, dtype=torch.int32, device=DEV),
+            torch.full((w.rows, 16, 192), float("nan"), dtype=torch.bfloat16, device=DEV),
+            torch.zeros(sda.workspace_bytes(w.rows, 16, 2), dtype=torch.uint8, device=DEV))
+
+
+def _same(a, b):
+    return all(torch.equal(x.view(torch.int32) if x.dtype == torch.float32 else
+                           x.view(torch.int16) if x.dtype == torch.bfloat16 else x,
+                           y.view(torch.int32) if y.dtype == torch.float32 else
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y)
+               for x, y in zip(a[:5], b[:5]))
+
+
+def test_decode_chain_graph_replay_matches_eager():
+    """The whole decode step (tensor-core indexer, selection, split attention + combine)
+    captured in one CUDA graph: its replays write the eager step's bits (scores, metadata,
+    ids, output), so no kernel of the chain depends on host state or on a previous call."""
+    w = inputs.make_index_workload(DEV, requests=5, groups=4, query_len=2, ctx=(9000, 30000), block=64, seed=21)
+    cache, query, positions, active = _chain_inputs(w, 22)
+    topk = 256
+    eager = _chain_bufs(w, topk)
+    _chain_step(w, cache, query, positions, active, topk, eager, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graphed = _chain_bufs(w, topk)
+    stream = torch.cuda.Stream(DEV)
+    stream.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        _chain_step(w, cache, query, positions, active, topk, graphed, stream)   # warm-up
+        stream.synchronize()
+        for t in graphed[:5]:
+            t.fill_(0)
+        with torch.cuda.graph(g, stream=stream):
+            _chain_step(w, cache, query, positions, active, topk, graphed, stream)
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        assert _same(graphed, eager)
+    assert sda.read_errors(eager[5]) == 0 and sda.read_errors(graphed[5]) == 0
+    ids = graphed[3].cpu().numpy()
+    assert np.array_equal(ids, oracle.select_regions(eager[0].cpu(), eager[1].cpu(), topk, eager[2].cpu()))
+
+
+def test_decode_chains_on_two_streams_at_once():
+    """Two decode steps on different inputs, interleaved on two streams with their own
+    buffers: each stream's results equal its step run alone (the library keeps no state
+    between calls that two streams could share)."""
+    ws_ = [inputs.make_index_workload(DEV, requests=4, groups=4, query_len=q, ctx=(6000, 20000), block=64,
+                                      seed=31 + q) for q in (1, 2)]
+    ins = [_chain_inputs(w, 40 + i) for i, w in enumerate(ws_)]
+    topk = 128
+    alone = []
+    for w, (cache, query, pos, act) in zip(ws_, ins):
+        b = _chain_bufs(w, topk)
+        _chain_step(w, cache, query, pos, act, topk, b, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        alone.append(b)
+    streams = [torch.cuda.Stream(DEV), torch.cuda.Stream(DEV)]
+    bufs = [_chain_bufs(w, topk) for w in ws_]
+    torch.cuda.synchronize()
+    for _ in range(10):
+        for w, (cache, query, pos, act), b, s in zip(ws_, ins, bufs, streams):
+            _chain_step(w, cache, query, pos, act, topk, b, s)
+    torch.cuda.synchronize()
+    for b, a in zip(bufs, alone):
+        assert _same(b, a)
+        assert sda.read_errors(b[5]) == 0
