@@ -23,7 +23,8 @@
 //     partial output and log-sum-exp for the combine kernel.
 // Window mode walks the pieces of [pos - window + 1, pos] instead of regions;
 // with token pairs one CTA serves two query tokens of a request (their
-// overlapping windows streamed once, one warp pair per token).
+// overlapping windows streamed once, one warp pair per token; with a bf16
+// cache the two warps of a token take alternate stages, all slots each).
 // Every mbarrier wait is bounded; a wait that runs out raises a flag in the
 // workspace header and the CTA winds down after its copies have landed.
 #include <cuda.h>
@@ -453,7 +454,8 @@ __device__ __forceinline__ void pv_accumulate(float (&o)[24][4], const uint32_t 
 // query_len): a CTA serves two consecutive query tokens of a request and
 // group, whose windows are one token apart; the producer streams (its split's
 // share of) their union once, each warp pair computes one token over every
-// stage and writes that token's row (output, or partial and LSE).
+// stage (bf16: its two warps on alternate stages) and writes that token's row
+// (output, or partial and LSE).
 template <bool FP8, bool WINDOW, bool FULL, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 2)
     sda_split_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ Params p)
@@ -487,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             for (int s = 0; s < T::kStages; ++s) {
                 mbar_init(full_bar + 8 * s, 1);
-                mbar_init(empty_bar + 8 * s, PAIR ? kConsumerWarps : kWarpsPerStage);
+                mbar_init(empty_bar + 8 * s, (PAIR && FP8) ? kConsumerWarps : kWarpsPerStage);
             }
             mbar_init_fence();
             prefetch_tmap(&tmap);
@@ -802,15 +804,19 @@ __global__ void __launch_bounds__(kThreads, 2)
     float l_run[2] = {0.0f, 0.0f};
 
     // This warp's pair takes stages pair, pair + 2, ...; inside a stage it owns
-    // slots [slot0, slot0 + kWarpTokens): NT token tiles of 8 for QK^T and KS
-    // k-steps of 16 for PV.
-    constexpr int NT = T::kWarpTokens / 8;
-    constexpr int KS = T::kWarpTokens / 16;
-    // PAIR: both warp pairs take every stage, pair k serving token k.
-    const int pair = PAIR ? 0 : warp / kWarpsPerStage;
+    // slots [slot0, slot0 + WT): NT token tiles of 8 for QK^T and KS k-steps
+    // of 16 for PV.  PAIR: warps 2k and 2k + 1 serve token k; with FP8 both
+    // take every stage (half its slots each), with bf16 (ALT) they take
+    // alternate stages, all 32 slots each: four independent score tiles per
+    // warp instead of two, and two arrivals per stage instead of four.
+    constexpr bool ALT = PAIR && !FP8;
+    constexpr int WT = ALT ? T::kSlots : T::kWarpTokens;
+    constexpr int NT = WT / 8;
+    constexpr int KS = WT / 16;
+    const int pair = ALT ? (warp & 1) : PAIR ? 0 : warp / kWarpsPerStage;
     const uint64_t *my_hdr = hdr + (PAIR ? (warp >> 1) * T::kStages : 0);
-    const int slot0 = (warp % kWarpsPerStage) * T::kWarpTokens;
-    constexpr uint64_t kWarpMask = (T::kWarpTokens >= 64) ? ~0ull : ((1ull << T::kWarpTokens) - 1ull);
+    const int slot0 = ALT ? 0 : (warp % kWarpsPerStage) * T::kWarpTokens;
+    constexpr uint64_t kWarpMask = (WT >= 64) ? ~0ull : ((1ull << WT) - 1ull);
 
     // Per-lane part of the V ldmatrix addresses: matrix mi = lane / 8 covers
     // k-slots (mi & 1) * 8 + 0..7 of chunk (mi >> 1) of the chunk pair.
@@ -834,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                              : tile_offset(slot0 + 16 * k2 + (vk & 8), piece_c, pps_c, pstride)) +
                        vsw * 128u;
 
-    for (int st = pair; st < n_st; st += PAIR ? 1 : kPairs) {
+    for (int st = pair; st < n_st; st += ALT ? 2 : PAIR ? 1 : kPairs) {
         const int s = st % T::kStages;
         const uint32_t par = static_cast<uint32_t>(st / T::kStages) & 1u;
         const bool ok = mbar_wait(full_bar + 8 * s, par, p.wait_ns);
