@@ -1122,46 +1122,66 @@ constexpr int kCombineThreads = kMaxHeads * (kDim / 4);   // 768
 __global__ void __launch_bounds__(kCombineThreads) sda_combine_kernel(const __grid_constant__ Params p)
 {
     SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, kTimelineCombine + blockIdx.x * 2ull);
-    pdl_wait();   // partials come from the split kernel
-    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, kTimelineCombine + blockIdx.x * 2ull + 1);
     const int row = blockIdx.x;
     const int item = threadIdx.x;
-    if (item >= p.heads * (kDim / 4))
-        return;
-    const int h = item / (kDim / 4);
+    const bool mine = item < p.heads * (kDim / 4);
+    const int h = mine ? item / (kDim / 4) : 0;
     const int d = 4 * (item - h * (kDim / 4));
+    // Inputs the split kernel does not write (activity, gate) are read while it
+    // still runs; its partials and LSEs only after the wait.
+    bool act = false;
+    float gam = 1.0f;
+    if (mine) {
+        act = p.window != 0 || p.active[row * p.act_s0] != 0;
+        if (act && p.gate)
+            gam = gate_factor(p.gate[(row / p.groups) * p.g_s0 +
+                                     static_cast<int64_t>((row % p.groups) * p.heads + h) * p.g_s1]);
+    }
+    pdl_wait();   // partials come from the split kernel
+    SDA_STAMP(threadIdx.x == 0 && blockIdx.x < kTimelineUnits, kTimelineCombine + blockIdx.x * 2ull + 1);
+    if (!mine)
+        return;
     uint16_t *out = p.output + static_cast<int64_t>(row) * p.o_s0 + static_cast<int64_t>(h) * p.o_s1 + d;
-    if (p.window == 0 && p.active[row * p.act_s0] == 0) {
+    if (!act) {
         if (p.clear_inactive)
             out[0] = out[1] = out[2] = out[3] = 0;
         return;
     }
     const int S = p.splits;
     const float *l = p.lse + static_cast<int64_t>(row) * S * p.heads + h;
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s)
-        M = fmaxf(M, l[s * p.heads]);
     const float4 *part = reinterpret_cast<const float4 *>(
         p.partial + (static_cast<int64_t>(row) * S * p.heads + h) * kDim + d);
     const int64_t step = static_cast<int64_t>(p.heads) * (kDim / 4);   // float4s between splits
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     float wsum = 0.0f;
-    if (M != -INFINITY) {
-#pragma unroll 4
-        for (int s = 0; s < S; ++s) {
-            const float w = expf(l[s * p.heads] - M);
-            const float4 v = part[s * step];
+    // splits in groups of 4: a group's LSEs and partials load together
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s)
+        M = S <= 4 ? M : fmaxf(M, l[s * p.heads]);
+    for (int s0 = 0; s0 < S; s0 += 4) {
+        float lv[4];
+        float4 pv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            lv[j] = s0 + j < S ? l[(s0 + j) * p.heads] : -INFINITY;
+            pv[j] = s0 + j < S ? part[(s0 + j) * step] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+        if (S <= 4)
+            M = fmaxf(fmaxf(lv[0], lv[1]), fmaxf(lv[2], lv[3]));
+        if (M == -INFINITY)
+            break;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (lv[j] == -INFINITY)
+                continue;
+            const float w = expf(lv[j] - M);
             wsum += w;
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
+            acc.x += w * pv[j].x;
+            acc.y += w * pv[j].y;
+            acc.z += w * pv[j].z;
+            acc.w += w * pv[j].w;
         }
     }
-    const int64_t tok = row / p.groups;
-    const int grp = row % p.groups;
-    const float gam = p.gate ? gate_factor(p.gate[tok * p.g_s0 + static_cast<int64_t>(grp * p.heads + h) * p.g_s1])
-                             : 1.0f;
     const float f = wsum > 0.0f ? gam / wsum : 0.0f;
     out[0] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.x * f));
     out[1] = __bfloat16_as_ushort(__float2bfloat16_rn(acc.y * f));
